@@ -1,0 +1,728 @@
+/*
+ * emu_oracle.c -- exact-integer CPU oracle for the emulated FP8 scaled GEMM.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE. Only the test suite, the smoke check and
+ * the benchmark's CPU-baseline leg load this library. It shares no code, header,
+ * table or helper with the CUDA library; neither side includes or links the other.
+ *
+ * What it computes: the FP8 GEMM out = (A @ B) * scale_a * scale_b of a reference
+ * tensor-core platform, as the mmaemu v0.1 documentation describes it.  Sources,
+ * cited by page title and section/table:
+ *
+ *  [UG-1]  "User guide", section 1 "What mmaemu does, in one paragraph":
+ *          blocks of products aligned to the block's largest exponent and truncated;
+ *          split-K partial sums; an epilogue that rounds twice.
+ *  [UG-3]  "User guide", section 3 "A first GEMM": operand layouts (mat1 [M,K]
+ *          row-major, mat2 [K,N] column-major), tensor-wise scales multiply the result.
+ *  [VAL-CL] "Validation evidence", table "Claims and their recordings":
+ *          zero products are left out of the block maximum; subnormal inputs keep the
+ *          exponent emin; an all-zero block still truncates c; exact zeros are +0;
+ *          terms and block sums are truncated to 13 fraction bits (alignment, carry,
+ *          sign-magnitude truncation); 64-wide k-tiles dealt round-robin to the splits;
+ *          serial or pairwise combination, S = 3 pairwise is (p2 + p0) + p1;
+ *          bf16/fp16 outputs rounded from the fp32 value; canonical NaN outputs.
+ *  [VAL-H] "Validation evidence", table of the H100 PCIe probe's claims:
+ *          32-product blocks, 13 fraction bits, c entering the block's alignment;
+ *          slow accumulation restarts every 128 elements and adds chunk results in K
+ *          order; split-K in contiguous runs of 128-wide k-tiles added serially;
+ *          epilogue RN(RN32(acc * RN32(sa * sb))).
+ *  [VAL-S] "Validation evidence", table "Scope": rows "Ada instruction model" (a block
+ *          result that is exactly zero or truncates to zero is +0), "Hopper preset",
+ *          "Slow accumulation" (chunks per split when split), "Split-K on the H100
+ *          PCIe" (a contiguous split without k-tiles), "Epilogue".
+ *  [LIM-C] "Limitations of mmaemu v0.1", section "Corrections of earlier statements":
+ *          y = fma(acc, alpha, +0); the interleaved split rule; the NaN rule (a NaN
+ *          code anywhere in row m of A or column n of B makes output (m, n) NaN).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - the exponent of a product is the label e_a + e_b (significands multiply to
+ *    [0, 4) without renormalisation), which is what makes a "carry" possible;
+ *  - c enters every block of a chain (one block is one instruction step);
+ *  - the block sum is truncated to F+1 significant bits below its own leading bit;
+ *  - Inf codes (E5M2) follow IEEE on the exact products: Inf*0 -> NaN,
+ *    +Inf and -Inf together -> NaN, otherwise the Inf survives every later sum;
+ *  - a contiguous split takes q = ceil(T/S) tiles, trailing splits may be empty;
+ *  - the pairwise tree for general S adds p[i] += p[i + h], h = ceil(S/2);
+ *  - canonical NaN is 0x7FC00000 (fp32), 0x7FC0 (bf16), 0x7E00 (fp16);
+ *  - a block result beyond the fp32 range becomes +-Inf (unreachable at real K).
+ *
+ * The model uses no floating-point arithmetic: every value is an integer
+ * significand times a power of two, and every rounding (fp32 round-to-nearest-even,
+ * bf16/fp16 rounding) is done on integers.  Host flush-to-zero therefore cannot
+ * affect it.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <pthread.h>
+#include <unistd.h>
+
+typedef __int128 i128;
+typedef unsigned __int128 u128;
+
+#define FMT_E4M3FN 0
+#define FMT_E5M2 1
+#define OUT_F32 0
+#define OUT_BF16 1
+#define OUT_F16 2
+#define MODE_RNE 0
+#define MODE_RZ 1
+
+/* status codes of the oracle's entry points */
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_EUNSUPPORTED (-3)
+#define ORC_ENOMEM (-5)
+
+typedef struct {
+  int32_t block_width;    /* B: products per block (32 hopper, 16 ada)            */
+  int32_t frac_bits;      /* F: retained fraction bits (13)                       */
+  int32_t restart;        /* R: slow-accumulation chunk length (128)              */
+  int32_t c_in_alignment; /* 1: c takes part in the block's alignment             */
+  int32_t split_scheme;   /* 0: contiguous k-tiles, 1: interleaved (round-robin)  */
+  int32_t ktile;          /* k-tile width of the split rule (128 hopper, 64 ada)  */
+  int32_t combine;        /* 0: serial, 1: pairwise                               */
+} orc_preset_t;
+
+/* ------------------------------------------------------------------------- */
+/* FP8 decode (OCP 8-bit floating point formats; the emin rule is [VAL-CL]).   */
+/* value = (-1)^neg * sig * 2^(e - f); a subnormal keeps e = emin = 1 - bias.  */
+/* ------------------------------------------------------------------------- */
+typedef struct { int nan, inf, neg, sig, e, f; } fp8v;
+
+static fp8v fp8_decode(int fmt, unsigned code) {
+  fp8v d;
+  memset(&d, 0, sizeof d);
+  d.neg = (int)((code >> 7) & 1u);
+  if (fmt == FMT_E4M3FN) {          /* 1 sign, 4 exponent (bias 7), 3 fraction */
+    unsigned E = (code >> 3) & 15u, m = code & 7u;
+    d.f = 3;
+    if (E == 15u && m == 7u) { d.nan = 1; return d; }   /* S.1111.111; no Inf */
+    if (E == 0u) { d.sig = (int)m; d.e = 1 - 7; }
+    else { d.sig = 8 + (int)m; d.e = (int)E - 7; }
+  } else {                          /* 1 sign, 5 exponent (bias 15), 2 fraction */
+    unsigned E = (code >> 2) & 31u, m = code & 3u;
+    d.f = 2;
+    if (E == 31u) { if (m) d.nan = 1; else d.inf = 1; return d; }
+    if (E == 0u) { d.sig = (int)m; d.e = 1 - 15; }
+    else { d.sig = 4 + (int)m; d.e = (int)E - 15; }
+  }
+  return d;
+}
+
+/* one exact product: (-1)^neg * sig * 2^(e - f), label exponent e = e_a + e_b */
+typedef struct { int neg, sig, e, f; } prod_t;
+
+static prod_t make_product(const fp8v* a, const fp8v* b) {
+  prod_t p;
+  p.neg = a->neg ^ b->neg;
+  p.sig = a->sig * b->sig;
+  p.e = a->e + b->e;
+  p.f = a->f + b->f;
+  return p;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Integer rounding of an exact value (-1)^neg * mag * 2^exp2 into a binary     */
+/* format with p significand bits (hidden bit included), exponent range         */
+/* [emin, emax] and ebits exponent bits.  mode: nearest-even or toward zero.    */
+/* ------------------------------------------------------------------------- */
+static int bitlen128(u128 x) {
+  int n = 0;
+  while (x) { ++n; x >>= 1; }
+  return n;
+}
+
+static uint32_t round_to_format(int neg, u128 mag, int exp2, int p, int emin, int emax,
+                                int ebits, int mode) {
+  uint32_t sign = (uint32_t)neg << (ebits + p - 1);
+  if (mag == 0) return sign;
+  int L = bitlen128(mag);
+  int lead = exp2 + L - 1;                       /* exponent of the leading bit */
+  int qe = lead - (p - 1);                       /* exponent of one ulp         */
+  if (qe < emin - (p - 1)) qe = emin - (p - 1);  /* subnormals: fixed quantum   */
+  int shift = qe - exp2;
+  u128 q;
+  if (shift <= 0) {
+    q = mag << (-shift);                         /* exact: fewer than p bits    */
+  } else {
+    u128 rem, half;
+    int round_up = 0, below_half = 0;
+    if (shift > 128) { q = 0; rem = mag; half = 0; below_half = 1; }  /* half > 2^128 > mag */
+    else if (shift == 128) { q = 0; rem = mag; half = (u128)1 << 127; }
+    else { q = mag >> shift; rem = mag - (q << shift); half = (u128)1 << (shift - 1); }
+    if (mode == MODE_RNE && !below_half) {
+      if (rem > half) round_up = 1;
+      else if (rem == half && (q & 1)) round_up = 1;
+    }
+    if (round_up) q += 1;
+  }
+  if (q == ((u128)1 << p)) { q >>= 1; qe += 1; }  /* rounding carried a bit     */
+  uint32_t bias = (1u << (ebits - 1)) - 1u;
+  if (q == 0) return sign;
+  if (q < ((u128)1 << (p - 1))) {                 /* subnormal                   */
+    return sign | (uint32_t)q;
+  }
+  int e_lead = qe + p - 1;
+  if (e_lead > emax) {                            /* overflow                    */
+    if (mode == MODE_RNE) return sign | (((1u << ebits) - 1u) << (p - 1));
+    return sign | ((((1u << ebits) - 2u)) << (p - 1)) | ((1u << (p - 1)) - 1u);
+  }
+  uint32_t biased = (uint32_t)(e_lead + (int)bias);
+  uint32_t frac = (uint32_t)(q - ((u128)1 << (p - 1)));
+  return sign | (biased << (p - 1)) | frac;
+}
+
+static uint32_t round_f32(int neg, u128 mag, int exp2, int mode) {
+  return round_to_format(neg, mag, exp2, 24, -126, 127, 8, mode);
+}
+
+/* fp32 bit pattern -> class and exact value; class 0 finite, 1 Inf, 2 NaN */
+typedef struct { int cls, neg; uint32_t mag; int exp2; } f32v;
+
+static f32v f32_unpack(uint32_t b) {
+  f32v v;
+  uint32_t ex = (b >> 23) & 255u, fr = b & 0x7FFFFFu;
+  v.neg = (int)(b >> 31);
+  v.cls = 0;
+  if (ex == 255u) { v.cls = fr ? 2 : 1; v.mag = 0; v.exp2 = 0; return v; }
+  if (ex == 0u) { v.mag = fr; v.exp2 = -149; }
+  else { v.mag = fr | 0x800000u; v.exp2 = (int)ex - 150; }
+  return v;
+}
+
+#define F32_CANON_NAN 0x7FC00000u
+#define F32_PINF 0x7F800000u
+
+/* RN32(a + b): IEEE single addition, round to nearest even, done on integers. */
+static uint32_t f32_add_rn(uint32_t a, uint32_t b) {
+  f32v x = f32_unpack(a), y = f32_unpack(b);
+  if (x.cls == 2 || y.cls == 2) return F32_CANON_NAN;
+  if (x.cls == 1 && y.cls == 1) return (x.neg == y.neg) ? a : F32_CANON_NAN;
+  if (x.cls == 1) return a;
+  if (y.cls == 1) return b;
+  if (x.mag == 0 && y.mag == 0) return (x.neg && y.neg) ? 0x80000000u : 0u;
+  if (x.mag == 0) return b;
+  if (y.mag == 0) return a;
+  /* Exact sum on a common exponent.  When the exponents are more than 100 apart
+     the smaller operand lies far below the rounding position of the result; only
+     its sign and the fact that it is nonzero matter, so it is replaced by one unit
+     at 2^(larger exp2 - 100), which rounds identically (no tie can arise). */
+  f32v *hi = (x.exp2 >= y.exp2) ? &x : &y, *lo = (x.exp2 >= y.exp2) ? &y : &x;
+  u128 lo_mag = lo->mag;
+  int lo_exp = lo->exp2;
+  if (hi->exp2 - lo_exp > 100) { lo_mag = 1; lo_exp = hi->exp2 - 100; }
+  int d = hi->exp2 - lo_exp;
+  i128 sh = (i128)((u128)hi->mag << d);
+  i128 sl = (i128)lo_mag;
+  i128 s = (hi->neg ? -sh : sh) + (lo->neg ? -sl : sl);
+  if (s == 0) return 0u;                       /* x + (-x) = +0 in RN          */
+  int neg = s < 0;
+  return round_f32(neg, (u128)(neg ? -s : s), lo_exp, MODE_RNE);
+}
+
+/* RN32(a * b) */
+static uint32_t f32_mul_rn(uint32_t a, uint32_t b) {
+  f32v x = f32_unpack(a), y = f32_unpack(b);
+  int neg = x.neg ^ y.neg;
+  if (x.cls == 2 || y.cls == 2) return F32_CANON_NAN;
+  if (x.cls == 1 || y.cls == 1) {
+    if ((x.cls == 0 && x.mag == 0) || (y.cls == 0 && y.mag == 0)) return F32_CANON_NAN;
+    return F32_PINF | ((uint32_t)neg << 31);
+  }
+  u128 m = (u128)x.mag * (u128)y.mag;
+  if (m == 0) return (uint32_t)neg << 31;
+  return round_f32(neg, m, x.exp2 + y.exp2, MODE_RNE);
+}
+
+/* y = fma(acc, alpha, +0): the exact product rounded once; an exactly zero
+   product gives +0 because (+-0) + (+0) = +0 [LIM-C, VAL-CL epilogue rows]. */
+static uint32_t f32_fma_plus0(uint32_t acc, uint32_t alpha) {
+  f32v x = f32_unpack(acc), y = f32_unpack(alpha);
+  int neg = x.neg ^ y.neg;
+  if (x.cls == 2 || y.cls == 2) return F32_CANON_NAN;
+  if (x.cls == 1 || y.cls == 1) {
+    if ((x.cls == 0 && x.mag == 0) || (y.cls == 0 && y.mag == 0)) return F32_CANON_NAN;
+    return F32_PINF | ((uint32_t)neg << 31);
+  }
+  u128 m = (u128)x.mag * (u128)y.mag;
+  if (m == 0) return 0u;
+  return round_f32(neg, m, x.exp2 + y.exp2, MODE_RNE);
+}
+
+/* fp32 -> bf16, round to nearest even; NaN -> canonical 0x7FC0 */
+static uint16_t f32_to_bf16(uint32_t b) {
+  f32v v = f32_unpack(b);
+  if (v.cls == 2) return 0x7FC0u;
+  if (v.cls == 1) return (uint16_t)(0x7F80u | ((uint32_t)v.neg << 15));
+  return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 8, -126, 127, 8, MODE_RNE);
+}
+
+/* fp32 -> fp16, round to nearest even, overflow -> Inf; NaN -> canonical 0x7E00 */
+static uint16_t f32_to_f16(uint32_t b) {
+  f32v v = f32_unpack(b);
+  if (v.cls == 2) return 0x7E00u;
+  if (v.cls == 1) return (uint16_t)(0x7C00u | ((uint32_t)v.neg << 15));
+  return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 11, -14, 15, 5, MODE_RNE);
+}
+
+/* ------------------------------------------------------------------------- */
+/* One block step [UG-1; VAL-CL "Zero products ..." and "Terms and block sums  */
+/* are truncated ..."; VAL-H "32-product blocks, 13 fraction bits, c entering   */
+/* the block's alignment"].                                                    */
+/*                                                                             */
+/*   E   = max of the label exponents of the nonzero products and e(c), c != 0 */
+/*   g   = 2^(E - F)                                                           */
+/*   t_i = sign_i * floor(|x_i| / g)   (each term truncated toward zero)       */
+/*   S   = t_c + sum t_i               (exact)                                 */
+/* Returns 0 when nothing is nonzero (the result is then +0), else 1 with S, E. */
+/* ------------------------------------------------------------------------- */
+static u128 shift_floor(u128 m, int sh) {      /* floor(m * 2^sh) for m >= 0 */
+  if (sh >= 0) return m << sh;
+  if (-sh >= 128) return 0;
+  return m >> (-sh);
+}
+
+static int blk_exact(uint32_t c_bits, const prod_t* p, int n, int F, i128* S_out, int* E_out) {
+  f32v c = f32_unpack(c_bits);
+  int have = 0, E = 0;
+  int c_nonzero = (c.mag != 0);
+  int ec = 0;
+  if (c_nonzero) {
+    /* c = Mc * 2^(ec - 23) with Mc < 2^24; a subnormal c keeps ec = -126 */
+    ec = c.exp2 + 23;
+    E = ec;
+    have = 1;
+  }
+  for (int i = 0; i < n; ++i) {
+    if (p[i].sig == 0) continue;               /* zero products: not in the max */
+    if (!have || p[i].e > E) E = p[i].e;
+    have = 1;
+  }
+  if (!have) return 0;
+  i128 S = 0;
+  if (c_nonzero) {
+    u128 t = shift_floor(c.mag, c.exp2 - E + F);
+    S += c.neg ? -(i128)t : (i128)t;
+  }
+  for (int i = 0; i < n; ++i) {
+    if (p[i].sig == 0) continue;
+    u128 t = shift_floor((u128)p[i].sig, p[i].e - p[i].f - E + F);
+    S += p[i].neg ? -(i128)t : (i128)t;
+  }
+  *S_out = S;
+  *E_out = E;
+  return 1;
+}
+
+/* blk(c, products): normalise S to F+1 significant bits (truncation toward zero),
+   result S * 2^(E - F) as fp32.  Exactly zero, or truncated to zero, gives +0. */
+static uint32_t blk(uint32_t c_bits, const prod_t* p, int n, int F) {
+  f32v c = f32_unpack(c_bits);
+  if (c.cls != 0) return c_bits;                /* Inf/NaN c is absorbing */
+  i128 S;
+  int E;
+  if (!blk_exact(c_bits, p, n, F, &S, &E)) return 0u;
+  if (S == 0) return 0u;
+  int neg = S < 0;
+  u128 mag = (u128)(neg ? -S : S);
+  int L = bitlen128(mag);
+  if (L > F + 1) {                              /* carry: keep F+1 bits */
+    int drop = L - (F + 1);
+    mag = (mag >> drop) << drop;
+  }
+  if (E - F + bitlen128(mag) - 1 > 127)          /* beyond fp32: +-Inf (reading) */
+    return F32_PINF | ((uint32_t)neg << 31);
+  /* exact for F <= 23: at most 24 significant bits, quantum 2^(E-F) >= 2^-149 */
+  return round_f32(neg, mag, E - F, MODE_RZ);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chains.  A chain is a sequence of products in K order.                      */
+/* Fast: c = +0, then c = blk(c, next B products) for consecutive groups of B   */
+/*       counted from the start of the chain [UG-1; UG-3 use_fast_accum].      */
+/* Slow: the chain is cut into chunks of R products; each chunk is a fast chain */
+/*       from +0; the chunk results are added in K order in fp32, RN [VAL-H].  */
+/* ------------------------------------------------------------------------- */
+static uint32_t chain_fast(const prod_t* p, int64_t len, int B, int F) {
+  uint32_t c = 0u;
+  for (int64_t i = 0; i < len; i += B) {
+    int n = (int)((len - i < B) ? (len - i) : B);
+    c = blk(c, p + i, n, F);
+  }
+  return c;
+}
+
+static uint32_t chain_slow(const prod_t* p, int64_t len, int B, int F, int R) {
+  uint32_t acc = 0u;
+  for (int64_t j = 0; j < len; j += R) {
+    int64_t n = (len - j < R) ? (len - j) : R;
+    uint32_t r = chain_fast(p + j, n, B, F);
+    acc = (j == 0) ? r : f32_add_rn(acc, r);
+  }
+  return acc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Split-K [VAL-H split claim; VAL-CL "Split-K assigns 64-wide k-tiles round-   */
+/* robin"; LIM-C].  Returns the K indices of split s in chain order.           */
+/* scheme 0 (contiguous): T = ceil(K/ktile) tiles; split s takes tiles         */
+/*   [s*q, min(T, (s+1)*q)), q = ceil(T/S); it may be empty.                   */
+/* scheme 1 (interleaved): tile t belongs to split t mod S, in increasing t.   */
+/* ------------------------------------------------------------------------- */
+static int64_t split_indices(int64_t K, int S, int scheme, int ktile, int s, int64_t* idx) {
+  int64_t T = (K + ktile - 1) / ktile, len = 0;
+  if (scheme == 0) {
+    int64_t q = (T + S - 1) / S;
+    int64_t t0 = (int64_t)s * q, t1 = (int64_t)(s + 1) * q;
+    if (t1 > T) t1 = T;
+    for (int64_t t = t0; t < t1; ++t)
+      for (int64_t k = t * ktile; k < (t + 1) * ktile && k < K; ++k) idx[len++] = k;
+  } else {
+    for (int64_t t = s; t < T; t += S)
+      for (int64_t k = t * ktile; k < (t + 1) * ktile && k < K; ++k) idx[len++] = k;
+  }
+  return len;
+}
+
+/* combine the S partials in fp32 RN: serial p0 + p1 + ... in index order, or the
+   pairwise tree p[i] += p[i + h], h = ceil(n/2), which gives (p2 + p0) + p1 at S=3 */
+static uint32_t combine_partials(uint32_t* part, int S, int pairwise) {
+  if (!pairwise) {
+    uint32_t acc = part[0];
+    for (int s = 1; s < S; ++s) acc = f32_add_rn(acc, part[s]);
+    return acc;
+  }
+  int n = S;
+  while (n > 1) {
+    int h = (n + 1) / 2;
+    for (int i = 0; i + h < n; ++i) part[i] = f32_add_rn(part[i], part[i + h]);
+    n = h;
+  }
+  return part[0];
+}
+
+/* ------------------------------------------------------------------------- */
+/* One output element (m, n): the fp32 accumulator before the scales.          */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  const uint8_t* A; int fa;       /* [M,K] row-major                   */
+  const uint8_t* B; int fb;       /* [K,N] column-major: B[k,n] at n*K+k */
+  int64_t M, N, K;
+  int fast, S;
+  orc_preset_t P;
+  fp8v lut_a[256], lut_b[256];
+} gemm_t;
+
+typedef struct { prod_t* prods; int64_t* idx; uint32_t* part; } scratch_t;
+
+static int scratch_init(scratch_t* w, int64_t K, int S) {
+  w->prods = (prod_t*)malloc(sizeof(prod_t) * (size_t)(K > 0 ? K : 1));
+  w->idx = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K > 0 ? K : 1));
+  w->part = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)S);
+  return (w->prods && w->idx && w->part) ? 0 : -1;
+}
+
+static void scratch_free(scratch_t* w) {
+  free(w->prods); free(w->idx); free(w->part);
+}
+
+static uint32_t acc_one(const gemm_t* g, int64_t m, int64_t n, scratch_t* w) {
+  const uint8_t* arow = g->A + m * g->K;
+  const uint8_t* bcol = g->B + n * g->K;
+  /* non-finite inputs: the NaN rule over the whole row and column [LIM-C], and the
+     IEEE reading for Inf codes */
+  int nan = 0, pinf = 0, ninf = 0;
+  for (int64_t k = 0; k < g->K; ++k) {
+    const fp8v* a = &g->lut_a[arow[k]];
+    const fp8v* b = &g->lut_b[bcol[k]];
+    if (a->nan || b->nan) { nan = 1; continue; }
+    if (a->inf || b->inf) {
+      int a_zero = (!a->inf && a->sig == 0), b_zero = (!b->inf && b->sig == 0);
+      if (a_zero || b_zero) nan = 1;
+      else if (a->neg ^ b->neg) ninf = 1;
+      else pinf = 1;
+    }
+  }
+  if (nan || (pinf && ninf)) return F32_CANON_NAN;
+  if (pinf) return F32_PINF;
+  if (ninf) return F32_PINF | 0x80000000u;
+
+  int B = g->P.block_width, F = g->P.frac_bits, R = g->P.restart;
+  for (int s = 0; s < g->S; ++s) {
+    int64_t len;
+    if (g->S == 1) {
+      len = g->K;
+      for (int64_t k = 0; k < len; ++k) w->idx[k] = k;
+    } else {
+      len = split_indices(g->K, g->S, g->P.split_scheme, g->P.ktile, s, w->idx);
+    }
+    for (int64_t i = 0; i < len; ++i) {
+      int64_t k = w->idx[i];
+      w->prods[i] = make_product(&g->lut_a[arow[k]], &g->lut_b[bcol[k]]);
+    }
+    w->part[s] = g->fast ? chain_fast(w->prods, len, B, F) : chain_slow(w->prods, len, B, F, R);
+  }
+  if (g->S == 1) return w->part[0];
+  return combine_partials(w->part, g->S, g->P.combine == 1);
+}
+
+/* epilogue [LIM-C; VAL-H]: alpha = RN32(sa*sb); y = fma(acc, alpha, +0);
+   bf16/fp16 rounded from y; NaN outputs canonical */
+static void epilogue_store(uint32_t acc, uint32_t alpha, int out_dtype, void* out, int64_t i) {
+  uint32_t y = f32_fma_plus0(acc, alpha);
+  if (out_dtype == OUT_F32) {
+    f32v v = f32_unpack(y);
+    ((uint32_t*)out)[i] = (v.cls == 2) ? F32_CANON_NAN : y;
+  } else if (out_dtype == OUT_BF16) {
+    ((uint16_t*)out)[i] = f32_to_bf16(y);
+  } else {
+    ((uint16_t*)out)[i] = f32_to_f16(y);
+  }
+}
+
+static int check_args(int fa, int fb, int64_t M, int64_t N, int64_t K, int S, const orc_preset_t* P) {
+  if (fa < 0 || fa > 1 || fb < 0 || fb > 1) return ORC_EINVAL;
+  if (M < 0 || N < 0 || K < 0 || S < 1 || !P) return ORC_EINVAL;
+  if (P->block_width < 1 || P->frac_bits < 0 || P->frac_bits > 23) return ORC_EUNSUPPORTED;
+  if (P->restart < P->block_width || P->restart % P->block_width) return ORC_EUNSUPPORTED;
+  if (P->ktile < 1) return ORC_EINVAL;
+  if (P->c_in_alignment != 1) return ORC_EUNSUPPORTED;
+  if (P->split_scheme < 0 || P->split_scheme > 1) return ORC_EINVAL;
+  if (P->combine < 0 || P->combine > 1) return ORC_EINVAL;
+  return ORC_OK;
+}
+
+static void gemm_setup(gemm_t* g, const uint8_t* A, int fa, const uint8_t* B, int fb,
+                       int64_t M, int64_t N, int64_t K, int fast, int S, const orc_preset_t* P) {
+  g->A = A; g->fa = fa; g->B = B; g->fb = fb;
+  g->M = M; g->N = N; g->K = K; g->fast = fast; g->S = S; g->P = *P;
+  for (int c = 0; c < 256; ++c) {
+    g->lut_a[c] = fp8_decode(fa, (unsigned)c);
+    g->lut_b[c] = fp8_decode(fb, (unsigned)c);
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Threaded drivers                                                             */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+  const gemm_t* g;
+  const int64_t* im; const int64_t* in;  /* sample lists, or NULL for the full grid */
+  int64_t count, begin, end;
+  uint32_t* acc_out;
+  int status;
+} job_t;
+
+static void* job_run(void* arg) {
+  job_t* j = (job_t*)arg;
+  scratch_t w;
+  if (scratch_init(&w, j->g->K, j->g->S)) { j->status = ORC_ENOMEM; scratch_free(&w); return NULL; }
+  for (int64_t i = j->begin; i < j->end; ++i) {
+    int64_t m, n;
+    if (j->im) { m = j->im[i]; n = j->in[i]; }
+    else { m = i / j->g->N; n = i % j->g->N; }
+    j->acc_out[i] = acc_one(j->g, m, n, &w);
+  }
+  scratch_free(&w);
+  j->status = ORC_OK;
+  return NULL;
+}
+
+static int run_jobs(const gemm_t* g, const int64_t* im, const int64_t* in, int64_t count,
+                    uint32_t* acc_out, int nthreads) {
+  if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > count) nthreads = (int)(count > 0 ? count : 1);
+  pthread_t th[256];
+  job_t jobs[256];
+  int64_t per = (count + nthreads - 1) / nthreads;
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t].g = g; jobs[t].im = im; jobs[t].in = in; jobs[t].count = count;
+    jobs[t].begin = (int64_t)t * per;
+    jobs[t].end = jobs[t].begin + per < count ? jobs[t].begin + per : count;
+    if (jobs[t].begin > count) jobs[t].begin = count;
+    jobs[t].acc_out = acc_out;
+    jobs[t].status = ORC_ENOMEM;
+  }
+  for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, job_run, &jobs[t]);
+  int st = ORC_OK;
+  for (int t = 0; t < nthreads; ++t) {
+    pthread_join(th[t], NULL);
+    if (jobs[t].status != ORC_OK) st = jobs[t].status;
+  }
+  return st;
+}
+
+/* ========================================================================= */
+/* Exported entry points                                                      */
+/* ========================================================================= */
+
+/* Full GEMM: out[M,N] row-major in out_dtype (0 fp32, 1 bf16, 2 fp16).
+   scale_a_bits / scale_b_bits are the fp32 bit patterns of the tensor-wise scales. */
+int oracle_scaled_mm(const uint8_t* A, int fmt_a, const uint8_t* B, int fmt_b,
+                     int64_t M, int64_t N, int64_t K, uint32_t scale_a_bits, uint32_t scale_b_bits,
+                     int out_dtype, int fast_accum, int split_S, const orc_preset_t* preset,
+                     void* out, int nthreads) {
+  int st = check_args(fmt_a, fmt_b, M, N, K, split_S, preset);
+  if (st) return st;
+  if (out_dtype < 0 || out_dtype > 2) return ORC_EINVAL;
+  int64_t count = M * N;
+  if (count == 0) return ORC_OK;
+  gemm_t* g = (gemm_t*)malloc(sizeof(gemm_t));
+  uint32_t* acc = (uint32_t*)malloc(sizeof(uint32_t) * (size_t)count);
+  if (!g || !acc) { free(g); free(acc); return ORC_ENOMEM; }
+  gemm_setup(g, A, fmt_a, B, fmt_b, M, N, K, fast_accum, split_S, preset);
+  st = run_jobs(g, NULL, NULL, count, acc, nthreads);
+  if (st == ORC_OK) {
+    uint32_t alpha = f32_mul_rn(scale_a_bits, scale_b_bits);
+    for (int64_t i = 0; i < count; ++i) epilogue_store(acc[i], alpha, out_dtype, out, i);
+  }
+  free(g); free(acc);
+  return st;
+}
+
+/* fp32 accumulators (before the scales) of the listed outputs (m_i, n_i). */
+int oracle_acc_sampled(const uint8_t* A, int fmt_a, const uint8_t* B, int fmt_b,
+                       int64_t M, int64_t N, int64_t K, int fast_accum, int split_S,
+                       const orc_preset_t* preset, int64_t count, const int64_t* idx_m,
+                       const int64_t* idx_n, uint32_t* acc_out, int nthreads) {
+  int st = check_args(fmt_a, fmt_b, M, N, K, split_S, preset);
+  if (st) return st;
+  for (int64_t i = 0; i < count; ++i)
+    if (idx_m[i] < 0 || idx_m[i] >= M || idx_n[i] < 0 || idx_n[i] >= N) return ORC_EINVAL;
+  if (count == 0) return ORC_OK;
+  gemm_t* g = (gemm_t*)malloc(sizeof(gemm_t));
+  if (!g) return ORC_ENOMEM;
+  gemm_setup(g, A, fmt_a, B, fmt_b, M, N, K, fast_accum, split_S, preset);
+  st = run_jobs(g, idx_m, idx_n, count, acc_out, nthreads);
+  free(g);
+  return st;
+}
+
+/* the epilogue alone over a vector of accumulators */
+int oracle_epilogue(const uint32_t* acc, int64_t count, uint32_t scale_a_bits,
+                    uint32_t scale_b_bits, int out_dtype, void* out) {
+  if (out_dtype < 0 || out_dtype > 2 || count < 0) return ORC_EINVAL;
+  uint32_t alpha = f32_mul_rn(scale_a_bits, scale_b_bits);
+  for (int64_t i = 0; i < count; ++i) epilogue_store(acc[i], alpha, out_dtype, out, i);
+  return ORC_OK;
+}
+
+/* decode one code: writes nan, inf, neg, sig, e, f */
+int oracle_decode(int fmt, int code, int32_t* out6) {
+  if (fmt < 0 || fmt > 1 || code < 0 || code > 255) return ORC_EINVAL;
+  fp8v d = fp8_decode(fmt, (unsigned)code);
+  out6[0] = d.nan; out6[1] = d.inf; out6[2] = d.neg; out6[3] = d.sig; out6[4] = d.e; out6[5] = d.f;
+  return ORC_OK;
+}
+
+/* the products of n code pairs, each as (neg, sig, e, f) */
+int oracle_products(int64_t n, const uint8_t* a, int fmt_a, const uint8_t* b, int fmt_b, int32_t* out4) {
+  for (int64_t i = 0; i < n; ++i) {
+    fp8v x = fp8_decode(fmt_a, a[i]), y = fp8_decode(fmt_b, b[i]);
+    prod_t p = make_product(&x, &y);
+    out4[4 * i] = p.neg; out4[4 * i + 1] = p.sig; out4[4 * i + 2] = p.e; out4[4 * i + 3] = p.f;
+  }
+  return ORC_OK;
+}
+
+/* blk over many independent blocks: block j has c = c_bits[j] and the n products
+   a[j*n + i] x b[j*n + i]; out[j] = fp32 bits of the block result.  F <= 23. */
+int oracle_blk_many(int64_t count, const uint32_t* c_bits, int n, const uint8_t* a, int fmt_a,
+                    const uint8_t* b, int fmt_b, int F, uint32_t* out) {
+  if (n < 0 || F < 0 || F > 23) return ORC_EINVAL;
+  prod_t* p = (prod_t*)malloc(sizeof(prod_t) * (size_t)(n > 0 ? n : 1));
+  if (!p) return ORC_ENOMEM;
+  for (int64_t j = 0; j < count; ++j) {
+    for (int i = 0; i < n; ++i) {
+      fp8v x = fp8_decode(fmt_a, a[j * n + i]), y = fp8_decode(fmt_b, b[j * n + i]);
+      p[i] = make_product(&x, &y);
+    }
+    out[j] = blk(c_bits[j], p, n, F);
+  }
+  free(p);
+  return ORC_OK;
+}
+
+/* the exact block sum S (as high/low 64-bit halves of an int128) and E, any F <= 96.
+   Returns 1 if the block has a nonzero member, 0 if not (S = 0, E = 0). */
+int oracle_blk_exact(uint32_t c_bits, int n, const uint8_t* a, int fmt_a, const uint8_t* b,
+                     int fmt_b, int F, int64_t* S_hi, uint64_t* S_lo, int32_t* E) {
+  if (n < 0 || n > 65536 || F < 0 || F > 96) return ORC_EINVAL;
+  prod_t* p = (prod_t*)malloc(sizeof(prod_t) * (size_t)(n > 0 ? n : 1));
+  if (!p) return ORC_ENOMEM;
+  for (int i = 0; i < n; ++i) {
+    fp8v x = fp8_decode(fmt_a, a[i]), y = fp8_decode(fmt_b, b[i]);
+    p[i] = make_product(&x, &y);
+  }
+  i128 S = 0;
+  int e = 0;
+  int r = blk_exact(c_bits, p, n, F, &S, &e);
+  free(p);
+  *S_hi = (int64_t)(S >> 64);
+  *S_lo = (uint64_t)S;
+  *E = e;
+  return r;
+}
+
+/* element-wise fp32 helpers over vectors (bit patterns) */
+int oracle_f32_add_rn(int64_t n, const uint32_t* a, const uint32_t* b, uint32_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_add_rn(a[i], b[i]);
+  return ORC_OK;
+}
+int oracle_f32_mul_rn(int64_t n, const uint32_t* a, const uint32_t* b, uint32_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_mul_rn(a[i], b[i]);
+  return ORC_OK;
+}
+int oracle_f32_fma_plus0(int64_t n, const uint32_t* a, const uint32_t* b, uint32_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_fma_plus0(a[i], b[i]);
+  return ORC_OK;
+}
+int oracle_f32_to_bf16(int64_t n, const uint32_t* a, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_bf16(a[i]);
+  return ORC_OK;
+}
+int oracle_f32_to_f16(int64_t n, const uint32_t* a, uint16_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_f16(a[i]);
+  return ORC_OK;
+}
+
+/* the K indices of split s, in chain order; returns the count */
+int64_t oracle_split_indices(int64_t K, int S, int scheme, int ktile, int s, int64_t* idx) {
+  if (K < 0 || S < 1 || s < 0 || s >= S || ktile < 1 || scheme < 0 || scheme > 1) return -1;
+  return split_indices(K, S, scheme, ktile, s, idx);
+}
+
+/* combine n partials (fp32 bits) serially or pairwise */
+uint32_t oracle_combine(const uint32_t* part, int S, int pairwise) {
+  uint32_t buf[4096];
+  if (S < 1 || S > 4096) return F32_CANON_NAN;
+  memcpy(buf, part, sizeof(uint32_t) * (size_t)S);
+  return combine_partials(buf, S, pairwise);
+}
+
+/* chains over an explicit code sequence (for pins): fast or slow */
+int oracle_chain(int64_t len, const uint8_t* a, int fmt_a, const uint8_t* b, int fmt_b,
+                 int fast, int B, int F, int R, uint32_t* out) {
+  if (len < 0 || B < 1 || F < 0 || F > 23 || R < B || R % B) return ORC_EINVAL;
+  prod_t* p = (prod_t*)malloc(sizeof(prod_t) * (size_t)(len > 0 ? len : 1));
+  if (!p) return ORC_ENOMEM;
+  for (int64_t i = 0; i < len; ++i) {
+    fp8v x = fp8_decode(fmt_a, a[i]), y = fp8_decode(fmt_b, b[i]);
+    p[i] = make_product(&x, &y);
+  }
+  *out = fast ? chain_fast(p, len, B, F) : chain_slow(p, len, B, F, R);
+  free(p);
+  return ORC_OK;
+}
+
+/* generic rounding of (-1)^neg * mag * 2^exp2 (mag = hi:lo) into fp32 (fmt 0),
+   bf16 (1) or fp16 (2), nearest-even (mode 0) or toward zero (mode 1) */
+uint32_t oracle_round(int neg, uint64_t mag_hi, uint64_t mag_lo, int exp2, int fmt, int mode) {
+  u128 mag = ((u128)mag_hi << 64) | mag_lo;
+  if (fmt == 0) return round_to_format(neg, mag, exp2, 24, -126, 127, 8, mode);
+  if (fmt == 1) return round_to_format(neg, mag, exp2, 8, -126, 127, 8, mode);
+  return round_to_format(neg, mag, exp2, 11, -14, 15, 5, mode);
+}

@@ -1,0 +1,97 @@
+"""ctypes binding of libemufp8 (include/emu_fp8.h): the C entry points under the
+same names, argument marshalling only.  Every step of the GEMM runs in the
+library's CUDA kernels; there is no Python or CPU fallback.  If the library is
+missing, every call raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+EMU_OK = 0
+EMU_EINVAL = -1
+EMU_EREJECT = -2
+EMU_EUNSUPPORTED = -3
+EMU_ECUDA = -4
+
+EMU_E4M3FN = 0
+EMU_E5M2 = 1
+EMU_OUT_F32 = 0
+EMU_OUT_BF16 = 1
+EMU_OUT_F16 = 2
+
+#: every symbol include/emu_fp8.h declares
+EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
+            "emu_abi_version")
+
+
+class emu_preset_t(ctypes.Structure):
+    _fields_ = [("block_width", ctypes.c_int32), ("frac_bits", ctypes.c_int32),
+                ("restart", ctypes.c_int32), ("c_in_alignment", ctypes.c_int32),
+                ("split_scheme", ctypes.c_int32), ("ktile", ctypes.c_int32),
+                ("combine", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_handle = None
+
+
+def load(path: str = LIB) -> ctypes.CDLL:
+    """Load libemufp8.so (raises OSError if it has not been built)."""
+    global _handle
+    if _handle is not None:
+        return _handle
+    if not os.path.exists(path):
+        raise OSError(f"libemufp8 is not built ({path} missing): run "
+                      "python -m bit_exact_fp8_gb300.build")
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    L.emu_preset_get.argtypes = [ctypes.c_char_p, ctypes.POINTER(emu_preset_t)]
+    L.emu_preset_get.restype = ctypes.c_int
+    L.emu_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
+    L.emu_workspace_bytes.restype = ctypes.c_size_t
+    L.emu_scaled_mm.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                ctypes.c_int64, P, P, P, ctypes.c_int, ctypes.c_int32,
+                                ctypes.c_int32, ctypes.POINTER(emu_preset_t), P, ctypes.c_size_t, P]
+    L.emu_scaled_mm.restype = ctypes.c_int
+    L.emu_last_error.argtypes = []
+    L.emu_last_error.restype = ctypes.c_char_p
+    L.emu_abi_version.argtypes = []
+    L.emu_abi_version.restype = ctypes.c_int
+    _handle = L
+    return L
+
+
+def emu_preset_get(name: str) -> emu_preset_t:
+    p = emu_preset_t()
+    st = load().emu_preset_get(name.encode(), ctypes.byref(p))
+    if st != EMU_OK:
+        raise KeyError(f"unknown preset {name!r}")
+    return p
+
+
+def emu_workspace_bytes(M: int, N: int, split_S: int) -> int:
+    return int(load().emu_workspace_bytes(M, N, split_S))
+
+
+def emu_last_error() -> str:
+    return load().emu_last_error().decode(errors="replace")
+
+
+def emu_abi_version() -> int:
+    return int(load().emu_abi_version())
+
+
+def emu_scaled_mm(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int, K: int,
+                  scale_a: int, scale_b: int, out: int, out_dtype: int, fast_accum: int,
+                  split_S: int, preset: emu_preset_t, workspace: int, workspace_bytes: int,
+                  stream: int) -> int:
+    """The C call with raw device addresses (ints); returns the status code."""
+    return int(load().emu_scaled_mm(
+        ctypes.c_void_p(A), fmt_a, ctypes.c_void_p(B), fmt_b, M, N, K,
+        ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(out), out_dtype,
+        int(fast_accum), int(split_S), ctypes.byref(preset), ctypes.c_void_p(workspace),
+        int(workspace_bytes), ctypes.c_void_p(stream)))

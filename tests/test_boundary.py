@@ -1,0 +1,132 @@
+"""CPU tests of the C ABI: the library loads, exports every symbol include/*.h
+declares, and its host-side checks return the documented status before any
+launch (no GPU is touched: every call here fails its argument checks first)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_exact_fp8_gb300 import _lib, build
+    build.build()
+    return _lib
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(emu_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = lib.load()
+    declared = declared_functions()
+    assert {"emu_scaled_mm", "emu_workspace_bytes", "emu_preset_get"} <= declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert set(lib.EXPORTED) == declared
+
+
+def test_presets_and_abi(lib):
+    assert lib.emu_abi_version() == 1
+    h = lib.emu_preset_get("hopper").as_dict()
+    assert h == dict(block_width=32, frac_bits=13, restart=128, c_in_alignment=1,
+                     split_scheme=0, ktile=128, combine=0)
+    a = lib.emu_preset_get("ada").as_dict()
+    assert a == dict(block_width=16, frac_bits=13, restart=128, c_in_alignment=1,
+                     split_scheme=1, ktile=64, combine=0)
+    with pytest.raises(KeyError):
+        lib.emu_preset_get("sm_120")
+    import oracle
+    assert oracle.PRESETS["hopper"] == h and oracle.PRESETS["ada"] == a
+
+
+def test_workspace_bytes(lib):
+    assert lib.emu_workspace_bytes(16, 256, 1) == 0
+    assert lib.emu_workspace_bytes(16, 256, 24) == 24 * 16 * 256 * 4
+    assert lib.emu_workspace_bytes(3, 16, 2) == 512          # rounded up to 256
+    assert lib.emu_workspace_bytes(-1, 16, 2) == 0
+
+
+FAKE = 1 << 20   # a 16-byte aligned non-null address; never dereferenced here
+
+
+def call(lib, **kw):
+    args = dict(A=FAKE, fmt_a=0, B=FAKE, fmt_b=0, M=16, N=64, K=256, scale_a=FAKE,
+                scale_b=FAKE, out=FAKE, out_dtype=1, fast_accum=1, split_S=1,
+                preset=lib.emu_preset_get("hopper"), workspace=0, workspace_bytes=0, stream=0)
+    args.update(kw)
+    return lib.emu_scaled_mm(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt_a=1, fmt_b=1), -2),                 # e5m2 x e5m2 rejected by torch
+    (dict(K=250), -2),                            # K not a multiple of 16
+    (dict(N=72), -2),                             # N not a multiple of 16
+    (dict(A=FAKE + 8), -2),                       # misaligned storage
+    (dict(out=FAKE + 4), -2),
+    (dict(fmt_a=2), -1),
+    (dict(out_dtype=3), -1),
+    (dict(M=-1), -1),
+    (dict(split_S=0), -1),
+    (dict(split_S=65), -3),
+    (dict(split_S=2), -1),                        # workspace missing
+    (dict(split_S=2, workspace=FAKE, workspace_bytes=100), -1),
+    (dict(scale_a=0), -1),
+    (dict(A=0), -1),
+    (dict(K=1 << 31), -3),
+])
+def test_argument_errors(lib, kw, status):
+    st = call(lib, **kw)
+    assert st == status, lib.emu_last_error()
+    assert lib.emu_last_error() != ""
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("block_width", 8, -3), ("frac_bits", 12, -3), ("c_in_alignment", 0, -3),
+    ("restart", 40, -3), ("ktile", 48, -3), ("split_scheme", 2, -1), ("combine", 2, -1)])
+def test_preset_errors(lib, field, value, status):
+    p = lib.emu_preset_get("hopper")
+    setattr(p, field, value)
+    assert call(lib, preset=p) == status
+
+
+def test_null_preset(lib):
+    L = lib.load()
+    st = L.emu_scaled_mm(None, 0, None, 0, 1, 16, 16, None, None, None, 0, 1, 1, None, None, 0, None)
+    assert st == -1
+
+
+def test_zero_sized_is_noop(lib):
+    # M == 0 or N == 0: success, nothing enqueued (no pointer needed)
+    assert call(lib, M=0, A=0, B=0, out=0, scale_a=0, scale_b=0) == 0
+    assert call(lib, N=0, A=0, B=0, out=0, scale_a=0, scale_b=0) == 0
+
+
+def test_python_api_rejects_cpu_and_unsupported():
+    from bit_exact_fp8_gb300 import (ReferenceRejectsError, UnsupportedFeatureError,
+                                     scaled_mm)
+    x = torch.zeros(16, 32).to(torch.float8_e4m3fn)
+    w = torch.zeros(16, 32).to(torch.float8_e4m3fn)
+    one = torch.ones(())
+    with pytest.raises(UnsupportedFeatureError):
+        scaled_mm(x, w.t(), one, one, bias=torch.zeros(16))
+    with pytest.raises(UnsupportedFeatureError):
+        scaled_mm(x, w.t(), one, one, scale_result=one)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm(x.float(), w.t(), one, one)
+    with pytest.raises(ValueError):                  # no CPU path
+        scaled_mm(x, w.t(), one, one)
+    assert issubclass(ReferenceRejectsError, RuntimeError)
+    assert issubclass(UnsupportedFeatureError, NotImplementedError)

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path (C ABI through the package binding) against the CPU
+oracle, bit for bit, on every workload -- at oracle-sized shapes that span several
+CTA tiles with ragged tails (full comparison), and at the full sizes in the
+configuration the benchmark times (sampled outputs, computed one by one by the
+oracle) -- plus the edge and degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+from bit_exact_fp8_gb300 import workloads as W
+from helpers import (assert_bits_equal, gpu_run, oracle_full, oracle_sampled,
+                     sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def full_check(cs, **kw):
+    a, b = W.make_inputs(cs)
+    got = gpu_run(cs, a, b, **kw)
+    want = oracle_full(cs, a, b, preset=kw.get("preset"))
+    assert_bits_equal(got, want, cs.name)
+
+
+def sampled_check(cs, count=256):
+    a, b = W.make_inputs(cs)
+    got = gpu_run(cs, a, b)
+    im, jn = sample_indices(cs.M, cs.N, count)
+    want = oracle_sampled(cs, a, b, im, jn)
+    assert_bits_equal(got[im, jn], want, cs.name + " (sampled)")
+    return got
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+def test_tiny_full():
+    full_check(W.case("tiny"))
+
+
+def test_linear_full():
+    full_check(W.case("linear"))
+
+
+@pytest.mark.parametrize("cs", W.CONFIGS["square"], ids=lambda c: c.name)
+def test_square_ragged_full(cs):
+    # several 128 x 64 tiles with ragged tails in M, N and K (K % 128 = 16)
+    full_check(W.shrink(cs, 200, 144, 1040))
+
+
+@pytest.mark.parametrize("cs", W.CONFIGS["square"][::2], ids=lambda c: c.name)
+def test_square_full_size_sampled(cs):
+    sampled_check(cs, count=96)
+
+
+@pytest.mark.parametrize("cs", W.CONFIGS["splitk"], ids=lambda c: c.name)
+def test_splitk_full_size_sampled(cs):
+    sampled_check(cs, count=64)
+
+
+@pytest.mark.parametrize("cs", [c for c in W.CONFIGS["splitk"] if c.out_dtype == "f32"],
+                         ids=lambda c: c.name)
+def test_splitk_ragged_full(cs):
+    # K not a multiple of the 128 (64) k-tile: the short tile is the last of its split
+    full_check(W.shrink(cs, 16, 64, 16384 + 48))
+
+
+@pytest.mark.parametrize("cs", W.CONFIGS["projection"], ids=lambda c: c.name)
+def test_projection_sampled_and_ragged(cs):
+    sampled_check(cs, count=128)
+    full_check(W.shrink(cs, 272, 208, 1920))
+
+
+# ---------------------------------------------------------------------------
+# presets x accumulation x output dtypes x formats on a ragged mid-size shape
+@pytest.mark.parametrize("preset", ("hopper", "ada"))
+@pytest.mark.parametrize("fast", (True, False))
+@pytest.mark.parametrize("od", ("f32", "bf16", "f16"))
+@pytest.mark.parametrize("fa,fb", (("e4m3fn", "e4m3fn"), ("e4m3fn", "e5m2"), ("e5m2", "e4m3fn")))
+def test_matrix(preset, fast, od, fa, fb):
+    cs = W.Case(f"matrix-{preset}-{fast}-{od}-{fa}-{fb}", 70, 96, 528, fa, fb, od, fast_accum=fast,
+                preset=preset, gen="mixed", seed=7)
+    full_check(cs)
+
+
+@pytest.mark.parametrize("S", (2, 3, 5, 8, 24, 64))
+@pytest.mark.parametrize("preset", ("hopper", "ada"))
+@pytest.mark.parametrize("pairwise", (False, True))
+def test_split_factors_and_combine(S, preset, pairwise):
+    if pairwise and preset == "hopper":
+        pytest.skip("the hopper preset combines serially")
+    P = dict(block_width=32, frac_bits=13, restart=128, c_in_alignment=1, split_scheme=0,
+             ktile=128, combine=0) if preset == "hopper" else \
+        dict(block_width=16, frac_bits=13, restart=128, c_in_alignment=1, split_scheme=1,
+             ktile=64, combine=int(pairwise))
+    for fast in (True, False):
+        cs = W.Case(f"split-{preset}-S{S}-{pairwise}-{fast}", 20, 48, 64 * 37 + 32, out_dtype="f32",
+                    fast_accum=fast, split_S=S, preset=preset, seed=9, sigma_a=8.0, sigma_b=8.0)
+        a, b = W.make_inputs(cs)
+        got = gpu_run(cs, a, b, preset=P)
+        want = oracle_full(cs, a, b, preset=P)
+        assert_bits_equal(got, want, cs.name)
+
+
+# ---------------------------------------------------------------------------
+# edge and degenerate cases
+def test_zero_dims_and_k0():
+    from bit_exact_fp8_gb300 import scaled_mm
+    dev = torch.device("cuda:0")
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    for M, N in ((0, 32), (8, 0)):
+        x = torch.zeros(M, 32, device=dev).to(torch.float8_e4m3fn)
+        w = torch.zeros(N, 32, device=dev).to(torch.float8_e4m3fn)
+        y = scaled_mm(x, w.t(), one, one, out_dtype=torch.bfloat16, use_fast_accum=True)
+        assert y.shape == (M, N)
+    x = torch.zeros(5, 0, device=dev).to(torch.float8_e4m3fn)
+    w = torch.zeros(16, 0, device=dev).to(torch.float8_e4m3fn)
+    y = scaled_mm(x, w.t(), one, -one, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int32), torch.zeros(5, 16, dtype=torch.int32, device=dev))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 16), (1, 16, 32), (3, 16, 48), (129, 80, 160),
+                                   (257, 16, 16), (5, 1024, 16)])
+def test_small_and_odd_shapes(M, N, K):
+    for fast in (True, False):
+        cs = W.Case(f"odd-{M}x{N}x{K}-{fast}", M, N, K, out_dtype="f32", fast_accum=fast,
+                    gen="mixed", seed=M + N + K)
+        full_check(cs)
+
+
+@pytest.mark.parametrize("fmt", ("e4m3fn", "e5m2"))
+def test_nan_rows_and_columns(fmt):
+    cs = W.Case("nan", 40, 48, 256, fmt, "e4m3fn", "f32", fast_accum=False, split_S=3, seed=2)
+    a, b = W.make_inputs(cs)
+    a[7, 100] = 0x7F if fmt == "e4m3fn" else 0x7E
+    b[13, 255] = 0xFF
+    got = gpu_run(cs, a, b)
+    want = oracle_full(cs, a, b)
+    assert_bits_equal(got, want, "nan")
+    assert (got[7] == 0x7FC00000).all() and (got[:, 13] == 0x7FC00000).all()
+
+
+def test_inf_codes_ieee_reading():
+    cs = W.Case("inf", 24, 32, 192, "e5m2", "e4m3fn", "f32", fast_accum=True, seed=3)
+    a, b = W.make_inputs(cs)
+    a[2, 10] = 0x7C            # +Inf
+    a[5, 11] = 0xFC            # -Inf
+    a[5, 40] = 0x7C            # +Inf and -Inf in one row -> NaN
+    b[:, 60] = 0x00
+    a[9, 60] = 0x7C            # Inf * 0 -> NaN
+    for od in ("f32", "bf16", "f16"):
+        c2 = W.Case("inf", 24, 32, 192, "e5m2", "e4m3fn", od, fast_accum=True, seed=3)
+        assert_bits_equal(gpu_run(c2, a, b), oracle_full(c2, a, b), f"inf {od}")
+
+
+def test_independent_of_out_buffer_and_deterministic():
+    cs = W.shrink(W.case("linear"), 64, 320, 1920)
+    a, b = W.make_inputs(cs)
+    want = oracle_full(cs, a, b)
+    for fill in (0x00, 0xFF, 0x7F):
+        assert_bits_equal(gpu_run(cs, a, b, prefill=fill), want, f"prefill {fill:#x}")
+
+
+def test_scales_zero_sign_and_specials():
+    cs = W.Case("scales", 32, 32, 128, out_dtype="f32", seed=4)
+    a, b = W.make_inputs(cs)
+    for sa, sb in ((1.0, -1.0), (0.0, 1.0), (-0.0, 1.0), (1e-30, 1e-20), (3.0, float("inf")),
+                   (float("nan"), 1.0), (1e-45, 1.0)):
+        for od in ("f32", "bf16", "f16"):
+            c2 = W.Case("scales", 32, 32, 128, out_dtype=od, scale_a=sa, scale_b=sb, seed=4)
+            assert_bits_equal(gpu_run(c2, a, b), oracle_full(c2, a, b), f"scales {sa} {sb} {od}")
+
+
+def test_rejections():
+    from bit_exact_fp8_gb300 import ReferenceRejectsError, UnsupportedFeatureError, scaled_mm
+    dev = torch.device("cuda:0")
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    x = torch.zeros(16, 32, device=dev).to(torch.float8_e5m2)
+    w = torch.zeros(16, 32, device=dev).to(torch.float8_e5m2)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm(x, w.t(), one, one)                      # e5m2 x e5m2
+    x4 = torch.zeros(16, 40, device=dev).to(torch.float8_e4m3fn)
+    w4 = torch.zeros(16, 40, device=dev).to(torch.float8_e4m3fn)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm(x4, w4.t(), one, one)                    # K % 16
+    x4 = torch.zeros(16, 32, device=dev).to(torch.float8_e4m3fn)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm(x4, x4, one, one)                        # mat2 row-major
+    with pytest.raises(UnsupportedFeatureError):
+        scaled_mm(x4, x4.t(), torch.ones(16, 1, device=dev), one)   # row-wise scale
+    with pytest.raises(UnsupportedFeatureError):
+        scaled_mm(x4, x4.t(), one, one, splitk=65)

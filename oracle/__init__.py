@@ -71,12 +71,18 @@ def build(force: bool = False) -> str:
 
 _lib = None
 
+#: tests may point the wrapper at another build of emu_oracle.c (a mutant copy)
+_LIB_OVERRIDE = os.environ.get("EMU_ORACLE_LIB")
+
 
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB_PATH)
+        if _LIB_OVERRIDE:
+            L = ctypes.CDLL(_LIB_OVERRIDE)
+        else:
+            build()
+            L = ctypes.CDLL(_LIB_PATH)
         P = ctypes.c_void_p
         i32, i64, u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
         L.oracle_scaled_mm.argtypes = [P, ctypes.c_int, P, ctypes.c_int, i64, i64, i64, u32, u32,

@@ -1,0 +1,95 @@
+"""Mutation check of the oracle's pins: copies of emu_oracle.c with one planted
+mistake each (on the CPU, in a temporary directory) must each fail the pin suite,
+and an unmutated copy must pass it.  A mutant that survives means a part of the
+method that no pin covers."""
+import os
+import shutil
+import subprocess
+import sys
+import tempfile
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "emu_oracle.c")
+
+# (name, original text, mutated text): each a plausible misreading or slip
+MUTANTS = [
+    ("zero products in the block max",
+     "    if (p[i].sig == 0) continue;               /* zero products: not in the max */",
+     "    /* zero products enter the max */"),
+    ("subnormal E4M3 without the emin label",
+     "if (E == 0u) { d.sig = (int)m; d.e = 1 - 7; }",
+     "if (E == 0u) { d.sig = (int)m; d.e = 0 - 7; }"),
+    ("c left out of the alignment",
+     "    E = ec;\n    have = 1;",
+     "    have = 0;"),
+    ("negative terms floored instead of truncated",
+     "    S += p[i].neg ? -(i128)t : (i128)t;",
+     "    S += p[i].neg ? -(i128)shift_floor((u128)p[i].sig * 2 + 1, p[i].e - p[i].f - E + F - 1) : (i128)t;"),
+    ("block sum kept to F bits, not F+1",
+     "  if (L > F + 1) {",
+     "  if (L > F) { L = L + 1;"),
+    ("slow chunks added in reverse K order",
+     "  for (int64_t j = 0; j < len; j += R) {\n    int64_t n = (len - j < R) ? (len - j) : R;",
+     "  for (int64_t j0 = 0; j0 < len; j0 += R) {\n    int64_t j = ((len - 1) / R) * R - j0;\n"
+     "    int64_t n = (len - j < R) ? (len - j) : R;"),
+    ("slow restart every R/2",
+     "    uint32_t r = chain_fast(p + j, n, B, F);\n    acc = (j == 0)",
+     "    uint32_t r = f32_add_rn(chain_fast(p + j, n / 2, B, F), chain_fast(p + j + n / 2, n - n / 2, B, F));\n    acc = (j == 0)"),
+    ("serial combine from the last split",
+     "    for (int s = 1; s < S; ++s) acc = f32_add_rn(acc, part[s]);",
+     "    acc = part[S - 1]; for (int s = S - 2; s >= 0; --s) acc = f32_add_rn(acc, part[s]);"),
+    ("epilogue without the +0 addend (keeps -0)",
+     "  if (m == 0) return 0u;\n  return round_f32(neg, m, x.exp2 + y.exp2, MODE_RNE);\n}\n\n/* fp32 -> bf16",
+     "  if (m == 0) return (uint32_t)neg << 31;\n  return round_f32(neg, m, x.exp2 + y.exp2, MODE_RNE);\n}\n\n/* fp32 -> bf16"),
+    ("pairwise tree with h = floor(n/2)",
+     "    int h = (n + 1) / 2;",
+     "    int h = n / 2;"),
+    ("balanced contiguous split",
+     "    int64_t q = (T + S - 1) / S;",
+     "    int64_t q = T / S + (s < T % S);"),
+    ("truncated zero block result as -0",
+     "  if (S == 0) return 0u;\n  int neg = S < 0;",
+     "  if (S == 0) return 0x80000000u;\n  int neg = S < 0;"),
+    ("bf16 rounded toward zero",
+     "return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 8, -126, 127, 8, MODE_RNE);",
+     "return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 8, -126, 127, 8, MODE_RZ);"),
+]
+
+
+def _build(src_text: str, out_dir: str, name: str) -> str:
+    c = os.path.join(out_dir, name + ".c")
+    so = os.path.join(out_dir, name + ".so")
+    with open(c, "w") as f:
+        f.write(src_text)
+    subprocess.check_call(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-pthread", c, "-o", so])
+    return so
+
+
+def _pins_pass(so: str) -> bool:
+    env = dict(os.environ, EMU_ORACLE_LIB=so)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    return r.returncode == 0
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc needed")
+def test_every_mutant_is_killed_and_the_identity_survives():
+    src = open(SRC).read()
+    tmp = tempfile.mkdtemp(prefix="oracle_mutants_")
+    try:
+        jobs = [("identity", _build(src, tmp, "identity"))]
+        for i, (name, old, new) in enumerate(MUTANTS):
+            assert src.count(old) == 1, f"mutation site not unique or missing: {name}"
+            jobs.append((name, _build(src.replace(old, new), tmp, f"m{i}")))
+        workers = max(1, min(len(jobs), (os.cpu_count() or 2)))
+        with ThreadPoolExecutor(workers) as ex:
+            results = dict(zip([n for n, _ in jobs], ex.map(lambda j: _pins_pass(j[1]), jobs)))
+        assert results.pop("identity"), "the unmutated oracle copy must pass its pins"
+        survivors = [n for n, passed in results.items() if passed]
+        assert not survivors, f"mutants not killed by any pin: {survivors}"
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)

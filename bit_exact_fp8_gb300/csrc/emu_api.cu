@@ -6,7 +6,10 @@
 #include "emu_fp8.h"
 #include "emu_kernels.cuh"
 
+#include <algorithm>
+#include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -28,31 +31,86 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tile shapes (thread tile TM x TN, CTA WM x WN threads).  The large tile for big
-// M x N; smaller ones keep the grid at a few CTAs per SM for skinny shapes.
-enum TileKind { kTileLarge = 0, kTileMid = 1, kTileSmall = 2 };
+// Tile shapes (thread tile TM x TN, CTA WM x WN threads):
+//   L    8 x 4, 16 x 16 threads: 128 x 64 outputs per CTA (large M x N)
+//   M40  4 x 2, 16 x 20 threads:  64 x 40 (M <= 64 with wide N: one CTA per SM)
+//   M32  4 x 4, 16 x  8 threads:  64 x 32
+//   S    2 x 2,  8 x 16 threads:  16 x 32 (skinny, split-K)
+struct TileInfo {
+  const char* name;
+  int bm, bn, threads, resident;  // resident CTAs per SM assumed by the cost model
+  double cost;                    // relative instructions per MAC (operand loads per MAC)
+};
+constexpr TileInfo kTiles[] = {
+    {"L", 128, 64, 256, 2, 1.00},
+    {"M40", 64, 40, 320, 1, 1.15},
+    {"M32", 64, 32, 128, 3, 1.05},
+    {"S", 16, 32, 128, 4, 1.50},
+};
+constexpr int kNumTiles = 4;
+constexpr int kSMs = 152;
 
-template <int TM, int TN, int WM, int WN>
-int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
-  constexpr int BM = WM * TM, BN = WN * TN;
-  dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)((p.M + BM - 1) / BM), (unsigned)p.S);
-  dim3 block(WM * WN);
-  if (blk == 32) {
-    if (slow) emu::emu_gemm_kernel<TM, TN, WM, WN, 32, true><<<grid, block, 0, st>>>(p);
-    else emu::emu_gemm_kernel<TM, TN, WM, WN, 32, false><<<grid, block, 0, st>>>(p);
-  } else {
-    if (slow) emu::emu_gemm_kernel<TM, TN, WM, WN, 16, true><<<grid, block, 0, st>>>(p);
-    else emu::emu_gemm_kernel<TM, TN, WM, WN, 16, false><<<grid, block, 0, st>>>(p);
+template <int TM, int TN, int WM, int WN, int BLK, bool SLOW>
+int launch_one(const emu::GemmParams& p, cudaStream_t st) {
+  using TS = emu::TileShape<TM, TN, WM, WN>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BLK, SLOW>;
+  // the dynamic shared memory limit is a per-function, per-device attribute
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM_BYTES);
+    if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)((p.M + TS::BM - 1) / TS::BM),
+            (unsigned)p.S);
+  kern<<<grid, TS::NT, TS::SMEM_BYTES, st>>>(p);
   return 0;
 }
 
+template <int TM, int TN, int WM, int WN>
+int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
+  if (blk == 32) {
+    return slow ? launch_one<TM, TN, WM, WN, 32, true>(p, st) : launch_one<TM, TN, WM, WN, 32, false>(p, st);
+  }
+  return slow ? launch_one<TM, TN, WM, WN, 16, true>(p, st) : launch_one<TM, TN, WM, WN, 16, false>(p, st);
+}
+
+// Pick the tile with the lowest estimated time: waves of resident CTAs times the
+// work of one CTA, with a penalty when fewer than 8 warps per SM are in flight.
+// EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
+int choose_tile(const emu::GemmParams& p) {
+  static int forced = -2;
+  if (forced == -2) {
+    forced = -1;
+    const char* env = getenv("EMU_FP8_TILE");
+    if (env)
+      for (int t = 0; t < kNumTiles; ++t)
+        if (std::strcmp(env, kTiles[t].name) == 0) forced = t;
+  }
+  if (forced >= 0) return forced;
+  int best = 0;
+  double best_cost = 0.0;
+  for (int t = 0; t < kNumTiles; ++t) {
+    const TileInfo& ti = kTiles[t];
+    const double ctas = (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
+    const double slots = (double)kSMs * ti.resident;
+    const double waves = std::ceil(ctas / slots);
+    const double warps_per_sm = std::min(ctas, slots) * (ti.threads / 32) / kSMs;
+    const double penalty = warps_per_sm < 8.0 ? 8.0 / warps_per_sm : 1.0;
+    const double est = waves * ti.bm * ti.bn * ti.cost * ti.resident * penalty;
+    if (t == 0 || est < best_cost) { best = t; best_cost = est; }
+  }
+  return best;
+}
+
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
-  const int64_t ctas_large = ((p.N + 63) / 64) * ((p.M + 127) / 128) * p.S;
-  const int64_t ctas_mid = ((p.N + 31) / 32) * ((p.M + 63) / 64) * p.S;
-  if (p.M >= 128 && ctas_large >= 2 * 152) return launch_tile<8, 4, 16, 16>(p, blk, slow, st);
-  if (p.M >= 64 && ctas_mid >= 152) return launch_tile<4, 4, 16, 8>(p, blk, slow, st);
-  return launch_tile<2, 2, 8, 16>(p, blk, slow, st);
+  switch (choose_tile(p)) {
+    case 0: return launch_tile<8, 4, 16, 16>(p, blk, slow, st);
+    case 1: return launch_tile<4, 2, 16, 20>(p, blk, slow, st);
+    case 2: return launch_tile<4, 4, 16, 8>(p, blk, slow, st);
+    default: return launch_tile<2, 2, 8, 16>(p, blk, slow, st);
+  }
 }
 
 }  // namespace

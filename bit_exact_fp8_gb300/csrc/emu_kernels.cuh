@@ -123,14 +123,34 @@ __device__ __forceinline__ uint32_t c16_pair(float lo, float hi) {
 
 // ---------------------------------------------------------------------------
 // The GEMM kernel.  Thread tile TM x TN outputs; CTA WM x WN threads; K staged in
-// steps of BK = 32 codes; BLK products per block (16 or 32); SLOW: restart chunks.
+// steps of BK = 32 codes through two shared-memory buffers (decode of stage s+1
+// overlaps nothing but needs only one barrier per stage); BLK products per block
+// (16 or 32); SLOW: restart chunks.
+template <int TM, int TN, int WM, int WN>
+struct TileShape {
+  static constexpr int NT = WM * WN;
+  static constexpr int BM = WM * TM;
+  static constexpr int BN = WN * TN;
+  static constexpr int BK = 32;
+  // one stage buffer: A values [BK][BM] f32, A labels [BK][BM] u32 (label in both
+  // halves), B values [BK][BN] f32, B labels [BK][BN] i16
+  static constexpr int A_VAL = 0;
+  static constexpr int A_LAB = A_VAL + BK * BM * 4;
+  static constexpr int B_VAL = A_LAB + BK * BM * 4;
+  static constexpr int B_LAB = B_VAL + BK * BN * 4;
+  static constexpr int STAGE_BYTES = ((B_LAB + BK * BN * 2) + 127) / 128 * 128;
+  static constexpr int LUT_BYTES = 2 * 256 * 8;
+  static constexpr int SMEM_BYTES = 2 * STAGE_BYTES + LUT_BYTES;
+};
+
 template <int TM, int TN, int WM, int WN, int BLK, bool SLOW>
 __global__ void __launch_bounds__(WM * WN)
 emu_gemm_kernel(const GemmParams p) {
-  constexpr int NT = WM * WN;
-  constexpr int BM = WM * TM;
-  constexpr int BN = WN * TN;
-  constexpr int BK = 32;
+  using TS = TileShape<TM, TN, WM, WN>;
+  constexpr int NT = TS::NT;
+  constexpr int BM = TS::BM;
+  constexpr int BN = TS::BN;
+  constexpr int BK = TS::BK;
   constexpr int NBLK = BK / BLK;
   constexpr int A_CHUNKS = BM * BK / 16;
   constexpr int B_CHUNKS = BN * BK / 16;
@@ -138,16 +158,24 @@ emu_gemm_kernel(const GemmParams p) {
   constexpr int B_PER = (B_CHUNKS + NT - 1) / NT;
   static_assert(TN % 2 == 0, "labels are paired along N");
 
-  __shared__ __align__(16) float sAv[BK][BM];
-  __shared__ __align__(16) uint32_t sAl[BK][BM];
-  __shared__ __align__(16) float sBv[BK][BN];
-  __shared__ __align__(16) int16_t sBl[BK][BN];
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint2* lutA = reinterpret_cast<uint2*>(smem + 2 * TS::STAGE_BYTES);
+  uint2* lutB = lutA + 256;
 
   const int tid = threadIdx.x;
   const int ty = tid / WN, tx = tid % WN;
   const int64_t m0 = (int64_t)blockIdx.y * BM;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int s = blockIdx.z;
+
+  // decode tables: code -> (pre-scaled value bits, label) for each operand
+  for (int c = tid; c < 256; c += NT) {
+    float v; int lab;
+    decode_code((uint32_t)c, p.fmt_a, kPreA, v, lab);
+    lutA[c] = make_uint2(__float_as_uint(v), ((uint32_t)lab & 0xFFFFu) | ((uint32_t)lab << 16));
+    decode_code((uint32_t)c, p.fmt_b, kPreB, v, lab);
+    lutB[c] = make_uint2(__float_as_uint(v), (uint32_t)lab & 0xFFFFu);
+  }
 
   // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
   const int64_t K = p.K;
@@ -171,18 +199,12 @@ emu_gemm_kernel(const GemmParams p) {
     n_stages -= stages_per_tile - (len_last + BK - 1) / BK;
   }
 
-  auto stage_k = [&](int64_t st, int64_t& k, int& valid) {
-    const int64_t tl = st / stages_per_tile;
-    const int64_t t = t_begin + tl * t_stride;
-    k = t * kt + (st % stages_per_tile) * BK;
-    const int64_t rem = K - k;
-    valid = rem < BK ? (int)rem : BK;
-  };
-
   uint4 ra[A_PER], rb[B_PER];
   auto load_stage = [&](int64_t st) {
-    int64_t k; int valid;
-    stage_k(st, k, valid);
+    const int64_t tl = st / stages_per_tile;
+    const int64_t k = (t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK;
+    const int64_t rem = K - k;
+    const int valid = rem < BK ? (int)rem : BK;
 #pragma unroll
     for (int r = 0; r < A_PER; ++r) {
       const int c = tid + r * NT;
@@ -206,7 +228,12 @@ emu_gemm_kernel(const GemmParams p) {
       rb[r] = v;
     }
   };
-  auto store_stage = [&]() {
+  auto store_stage = [&](int buf) {
+    unsigned char* base = smem + buf * TS::STAGE_BYTES;
+    float* sAv = reinterpret_cast<float*>(base + TS::A_VAL);
+    uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);
+    float* sBv = reinterpret_cast<float*>(base + TS::B_VAL);
+    int16_t* sBl = reinterpret_cast<int16_t*>(base + TS::B_LAB);
 #pragma unroll
     for (int r = 0; r < A_PER; ++r) {
       const int c = tid + r * NT;
@@ -215,10 +242,9 @@ emu_gemm_kernel(const GemmParams p) {
         const uint32_t w[4] = {ra[r].x, ra[r].y, ra[r].z, ra[r].w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float v; int lab;
-          decode_code((w[j >> 2] >> (8 * (j & 3))) & 0xFFu, p.fmt_a, kPreA, v, lab);
-          sAv[h * 16 + j][row] = v;
-          sAl[h * 16 + j][row] = ((uint32_t)lab & 0xFFFFu) | ((uint32_t)lab << 16);
+          const uint2 d = lutA[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
+          sAv[(h * 16 + j) * BM + row] = __uint_as_float(d.x);
+          sAl[(h * 16 + j) * BM + row] = d.y;
         }
       }
     }
@@ -230,10 +256,9 @@ emu_gemm_kernel(const GemmParams p) {
         const uint32_t w[4] = {rb[r].x, rb[r].y, rb[r].z, rb[r].w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float v; int lab;
-          decode_code((w[j >> 2] >> (8 * (j & 3))) & 0xFFu, p.fmt_b, kPreB, v, lab);
-          sBv[h * 16 + j][col] = v;
-          sBl[h * 16 + j][col] = (int16_t)lab;
+          const uint2 d = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
+          sBv[(h * 16 + j) * BN + col] = __uint_as_float(d.x);
+          sBl[(h * 16 + j) * BN + col] = (int16_t)d.y;
         }
       }
     }
@@ -247,12 +272,20 @@ emu_gemm_kernel(const GemmParams p) {
     for (int j = 0; j < TN; ++j) { cp[i][j] = 0.0f; accs[i][j] = 0.0f; }
   int blocks_in_chunk = 0;
 
-  if (n_stages > 0) load_stage(0);
+  __syncthreads();                       // tables ready
+  if (n_stages > 0) {
+    load_stage(0);
+    store_stage(0);
+    if (n_stages > 1) load_stage(1);
+  }
+  __syncthreads();
+
   for (int64_t st = 0; st < n_stages; ++st) {
-    __syncthreads();
-    store_stage();
-    __syncthreads();
-    if (st + 1 < n_stages) load_stage(st + 1);
+    const unsigned char* base = smem + (st & 1) * TS::STAGE_BYTES;
+    const float* sAv = reinterpret_cast<const float*>(base + TS::A_VAL);
+    const uint32_t* sAl = reinterpret_cast<const uint32_t*>(base + TS::A_LAB);
+    const float* sBv = reinterpret_cast<const float*>(base + TS::B_VAL);
+    const uint32_t* sBl2 = reinterpret_cast<const uint32_t*>(base + TS::B_LAB);
 
 #pragma unroll
     for (int bb = 0; bb < NBLK; ++bb) {
@@ -267,10 +300,9 @@ emu_gemm_kernel(const GemmParams p) {
       for (int kk = 0; kk < BLK; ++kk) {
         uint32_t la[TM], lb[TN / 2];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) la[i] = sAl[k0 + kk][ty * TM + i];
+        for (int i = 0; i < TM; ++i) la[i] = sAl[(k0 + kk) * BM + ty * TM + i];
 #pragma unroll
-        for (int jp = 0; jp < TN / 2; ++jp)
-          lb[jp] = reinterpret_cast<const uint32_t*>(&sBl[k0 + kk][0])[tx * (TN / 2) + jp];
+        for (int jp = 0; jp < TN / 2; ++jp) lb[jp] = sBl2[((k0 + kk) * BN) / 2 + tx * (TN / 2) + jp];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -296,9 +328,9 @@ emu_gemm_kernel(const GemmParams p) {
       for (int kk = 0; kk < BLK; ++kk) {
         float a[TM], b[TN];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) a[i] = sAv[k0 + kk][ty * TM + i];
+        for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ty * TM + i];
 #pragma unroll
-        for (int j = 0; j < TN; ++j) b[j] = sBv[k0 + kk][tx * TN + j];
+        for (int j = 0; j < TN; ++j) b[j] = sBv[(k0 + kk) * BN + tx * TN + j];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -326,6 +358,12 @@ emu_gemm_kernel(const GemmParams p) {
         }
       }
     }
+    // decode the next stage into the other buffer, prefetch the one after
+    if (st + 1 < n_stages) {
+      store_stage((int)((st + 1) & 1));
+      if (st + 2 < n_stages) load_stage(st + 2);
+    }
+    __syncthreads();
   }
 
   // chain result (fp32 accumulator of this split)

@@ -184,16 +184,20 @@ def test_rejections():
     one = torch.ones((), dtype=torch.float32, device=dev)
     x = torch.zeros(16, 32, device=dev).to(torch.float8_e5m2)
     w = torch.zeros(16, 32, device=dev).to(torch.float8_e5m2)
+    bf = torch.bfloat16
     with pytest.raises(ReferenceRejectsError):
-        scaled_mm(x, w.t(), one, one)                      # e5m2 x e5m2
+        scaled_mm(x, w.t(), one, one, out_dtype=bf)        # e5m2 x e5m2
     x4 = torch.zeros(16, 40, device=dev).to(torch.float8_e4m3fn)
     w4 = torch.zeros(16, 40, device=dev).to(torch.float8_e4m3fn)
     with pytest.raises(ReferenceRejectsError):
-        scaled_mm(x4, w4.t(), one, one)                    # K % 16
+        scaled_mm(x4, w4.t(), one, one, out_dtype=bf)      # K % 16
     x4 = torch.zeros(16, 32, device=dev).to(torch.float8_e4m3fn)
     with pytest.raises(ReferenceRejectsError):
-        scaled_mm(x4, x4, one, one)                        # mat2 row-major
+        scaled_mm(x4, torch.zeros(32, 16, device=dev).to(torch.float8_e4m3fn), one, one,
+                  out_dtype=bf)                            # mat2 row-major [K, N]
     with pytest.raises(UnsupportedFeatureError):
-        scaled_mm(x4, x4.t(), torch.ones(16, 1, device=dev), one)   # row-wise scale
+        scaled_mm(x4, x4.t(), torch.ones(16, 1, device=dev), one, out_dtype=bf)  # row-wise
     with pytest.raises(UnsupportedFeatureError):
-        scaled_mm(x4, x4.t(), one, one, splitk=65)
+        scaled_mm(x4, x4.t(), one, one, out_dtype=bf, splitk=65)
+    with pytest.raises(UnsupportedFeatureError):
+        scaled_mm(x4, x4.t(), one, one)                    # fp8 output (torch default dtype)

@@ -23,7 +23,10 @@ EMU_OUT_F16 = 2
 
 #: every symbol include/emu_fp8.h declares
 EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
-            "emu_abi_version")
+            "emu_abi_version", "emu_scaled_mm_noalloc")
+
+#: size of the static scratch of emu_scaled_mm_noalloc (EMU_NOALLOC_SCRATCH_BYTES)
+EMU_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class emu_preset_t(ctypes.Structure):
@@ -57,6 +60,11 @@ def load(path: str = LIB) -> ctypes.CDLL:
                                 ctypes.c_int64, P, P, P, ctypes.c_int, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.POINTER(emu_preset_t), P, ctypes.c_size_t, P]
     L.emu_scaled_mm.restype = ctypes.c_int
+    L.emu_scaled_mm_noalloc.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_int64, P, P, P, ctypes.c_int,
+                                        ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.POINTER(emu_preset_t), P]
+    L.emu_scaled_mm_noalloc.restype = ctypes.c_int
     L.emu_last_error.argtypes = []
     L.emu_last_error.restype = ctypes.c_char_p
     L.emu_abi_version.argtypes = []
@@ -95,3 +103,14 @@ def emu_scaled_mm(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int, K: int
         ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(out), out_dtype,
         int(fast_accum), int(split_S), ctypes.byref(preset), ctypes.c_void_p(workspace),
         int(workspace_bytes), ctypes.c_void_p(stream)))
+
+
+def emu_scaled_mm_noalloc(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int, K: int,
+                          scale_a: int, scale_b: int, out: int, out_dtype: int, fast_accum: int,
+                          split_S: int, preset: emu_preset_t, stream: int) -> int:
+    """The C call that keeps split partials in the library's static device scratch
+    (for callers that cannot allocate a workspace); returns the status code."""
+    return int(load().emu_scaled_mm_noalloc(
+        ctypes.c_void_p(A), fmt_a, ctypes.c_void_p(B), fmt_b, M, N, K,
+        ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(out), out_dtype,
+        int(fast_accum), int(split_S), ctypes.byref(preset), ctypes.c_void_p(stream)))

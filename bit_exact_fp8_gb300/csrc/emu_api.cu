@@ -12,6 +12,7 @@
 #include <cstdlib>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 namespace {
@@ -111,6 +112,37 @@ int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
     case 2: return launch_tile<4, 4, 16, 8>(p, blk, slow, st);
     default: return launch_tile<2, 2, 8, 16>(p, blk, slow, st);
   }
+}
+
+// Static split-partial scratch of emu_scaled_mm_noalloc.  Device code never
+// names it; host code only learns its device address through
+// cudaGetSymbolAddress, once per device, and passes that address to the kernels
+// as their workspace.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[EMU_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// The device address of g_noalloc_scratch on the current device (looked up on
+// the first call per device, with that device current).
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(EMU_ECUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(EMU_EUNSUPPORTED, "device index %d above the static scratch table", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(EMU_ECUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return EMU_OK;
 }
 
 }  // namespace
@@ -224,6 +256,29 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(EMU_ECUDA, "CUDA launch failed: %s", cudaGetErrorString(e));
   return EMU_OK;
+}
+
+int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,
+                          int64_t M, int64_t N, int64_t K, const float* scale_a,
+                          const float* scale_b, void* out, emu_out_t out_dtype,
+                          int32_t fast_accum, int32_t split_S, const emu_preset_t* preset,
+                          void* stream) {
+  g_last_error.clear();
+  const size_t need = emu_workspace_bytes(M, N, split_S);
+  if (need > EMU_NOALLOC_SCRATCH_BYTES)
+    return fail(EMU_EUNSUPPORTED,
+                "split partials need %zu bytes; the static scratch holds %zu "
+                "(split_S * M * N must be <= %zu)",
+                need, (size_t)EMU_NOALLOC_SCRATCH_BYTES, (size_t)EMU_NOALLOC_SCRATCH_BYTES / 4);
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (need > 0) {
+    const int st = noalloc_scratch(&ws);
+    if (st != EMU_OK) return st;
+    ws_bytes = EMU_NOALLOC_SCRATCH_BYTES;
+  }
+  return emu_scaled_mm(A, fmt_a, B, fmt_b, M, N, K, scale_a, scale_b, out, out_dtype, fast_accum,
+                       split_S, preset, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -115,6 +115,47 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a,
                   void* workspace, size_t workspace_bytes,
                   void* stream);
 
+/*
+ * emu_scaled_mm_noalloc: emu_scaled_mm for callers that cannot allocate device
+ * memory. (This entry point is an addition of this library; the documentation
+ * pages have no counterpart.)
+ *
+ * emu_scaled_mm itself allocates nothing, but with split_S > 1 it needs a
+ * caller-owned workspace for the fp32 split partials.  Some callers have no way
+ * to get one: a plugin or custom-op interface that hands the library only the
+ * input and output buffers, code whose memory is fixed at start-up and that must
+ * not call cudaMalloc (or a caching allocator) later, or a host framework that
+ * owns every allocation on the device.  This entry point keeps the partials in a
+ * file-scope static device array of EMU_NOALLOC_SCRATCH_BYTES bytes instead, so
+ * the caller passes only inputs and outputs.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ * Arguments, layouts, ownership and status codes are those of emu_scaled_mm,
+ * without the workspace.  Limit: split_S * M * N * 4 bytes (rounded up to 256)
+ * must fit in EMU_NOALLOC_SCRATCH_BYTES (4 MiB: split_S * M * N <= 1,048,576);
+ * larger calls return EMU_EUNSUPPORTED before any launch.
+ *
+ * The array exists once per GPU that loads the library and is held until the
+ * process exits.  The first call on a device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and caches it: make that first
+ * call before any CUDA stream capture.  Every call on a device shares the one
+ * array and leaves its partials there; each call writes every partial before it
+ * reads it, so nothing needs clearing.  Calls whose kernels overlap on the GPU
+ * (on different streams, or from different host threads, without ordering
+ * between them) race on the array and may return wrong results: order them on
+ * one stream or serialise them.
+ */
+#define EMU_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a,
+                          const uint8_t* B, emu_fp8_t fmt_b,
+                          int64_t M, int64_t N, int64_t K,
+                          const float* scale_a, const float* scale_b,
+                          void* out, emu_out_t out_dtype,
+                          int32_t fast_accum, int32_t split_S,
+                          const emu_preset_t* preset,
+                          void* stream);
+
 /* Message of the last error returned on the calling host thread ("" if none). */
 const char* emu_last_error(void);
 

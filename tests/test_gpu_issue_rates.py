@@ -1,0 +1,26 @@
+"""The throughput assumptions of the GEMM kernel's design, measured on the GPU:
+a round-toward-zero FP32 multiply with subnormal results (the truncation step) and
+an FP32 add of subnormals (the exact block sum) issue at the rate of an ordinary
+FP32 multiply, i.e. subnormal operands cost nothing extra."""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_subnormal_fp32_paths_run_at_full_rate():
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    with tempfile.TemporaryDirectory() as tmp:
+        exe = os.path.join(tmp, "issue_rates")
+        subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                               os.path.join(HERE, "gpu_probes", "issue_rates.cu"), "-o", exe])
+        out = subprocess.run([exe], capture_output=True, text=True, timeout=120, check=True).stdout
+    rates = {k: float(v) for k, v in (line.split() for line in out.strip().splitlines())}
+    print(rates)
+    assert rates["fmul_rz_subnormal"] >= 0.95 * rates["fmul_rn_normal"]
+    assert rates["fadd_subnormal"] >= 0.95 * rates["fmul_rn_normal"]

@@ -54,6 +54,38 @@ def measured_peaks():
     return None
 
 
+KERNEL_SOURCES = ("bit_exact_fp8_gb300/csrc/emu_kernels.cuh", "bit_exact_fp8_gb300/csrc/emu_api.cu")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary of
+    this workload, if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"emu_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel source sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def alu_peak_tops(peaks):
     """Issue-slot peak of 32-bit lane operations: SMs x 128 lanes x max SM clock."""
     mhz = (peaks or {}).get("sm_max_mhz", 2070.0)
@@ -261,9 +293,8 @@ def run_gpu(args, cs):
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     t_sum = sum(kernel_ms) / 1e3
     if ws > 1:
-        t = torch.tensor([t_sum], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_sum = float(t.item())
+        from bit_exact_fp8_gb300.sharding import max_over_ranks
+        t_sum = max_over_ranks(t_sum)
 
     flops_step = 2.0 * cs.M * cs.N * cs.K
     value = ws * flops_step * args.steps / t_sum / 1e12
@@ -274,8 +305,9 @@ def run_gpu(args, cs):
     peaks = measured_peaks()
     peak, mhz = alu_peak_tops(peaks)
     achieved = OPS_PER_MAC * cs.M * cs.N * cs.K / (t_sum / args.steps) / 1e12
+    traffic = args.traffic if args.traffic is not None else profiled_traffic(args.workload)
     roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s",
-            "frac": achieved / peak, "traffic": args.traffic,
+            "frac": achieved / peak, "traffic": traffic,
             "note": f"{OPS_PER_MAC} lane-ops per MAC (algorithmic); peak = {SMS} SMs x "
                     f"{LANES_PER_SM} lanes x {mhz:.0f} MHz issue slots (recipe unit counts, "
                     "sm_max_mhz of MEASURED_PEAKS.json)"}

@@ -32,29 +32,35 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tile shapes (thread tile TM x TN, CTA WM x WN threads):
-//   L    8 x 4, 16 x 16 threads: 128 x 64 outputs per CTA (large M x N)
-//   M40  4 x 2, 16 x 20 threads:  64 x 40 (M <= 64 with wide N: one CTA per SM)
-//   M32  4 x 4, 16 x  8 threads:  64 x 32
-//   S    2 x 2,  8 x 16 threads:  16 x 32 (skinny, split-K)
+// Tile shapes (thread tile TM x TN, CTA WM x WN threads, K-stage BK):
+//   L    8 x 4, 16 x 16 threads, BK 32: 128 x 64 outputs per CTA (large M x N)
+//   M40  4 x 2, 16 x 20 threads, BK 64:  64 x 40 (M <= 64 with wide N: one CTA per SM)
+//   M32  4 x 4, 16 x  8 threads, BK 32:  64 x 32
+//   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32 (skinny, split-K)
+//   K8   1 x 2,  4 x  4 x 8 lanes, BK 32:  4 x  8, each block split over 8 lanes
+//   K4   1 x 2,  4 x  8 x 4 lanes, BK 32:  4 x 16, each block split over 4 lanes
+//        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
+//        CTA tile must stay tiny for every SM to get work)
 struct TileInfo {
   const char* name;
-  int bm, bn, threads, resident;  // resident CTAs per SM assumed by the cost model
-  double cost;                    // relative instructions per MAC (operand loads per MAC)
+  int tm, tn, bm, bn, threads, resident, bk, g;  // resident: CTAs per SM for the cost model
+  double cost;                                   // relative instructions per MAC
 };
 constexpr TileInfo kTiles[] = {
-    {"L", 128, 64, 256, 2, 1.00},
-    {"M40", 64, 40, 320, 1, 1.15},
-    {"M32", 64, 32, 128, 3, 1.05},
-    {"S", 16, 32, 128, 4, 1.50},
+    {"L", 8, 4, 128, 64, 256, 2, 32, 1, 1.00},
+    {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15},
+    {"M32", 4, 4, 64, 32, 128, 3, 32, 1, 1.05},
+    {"S", 2, 2, 16, 32, 128, 4, 32, 1, 1.50},
+    {"K8", 1, 2, 4, 8, 128, 8, 32, 8, 3.00},
+    {"K4", 1, 2, 4, 16, 128, 8, 32, 4, 2.40},
 };
-constexpr int kNumTiles = 4;
+constexpr int kNumTiles = 6;
 constexpr int kSMs = 152;
 
-template <int TM, int TN, int WM, int WN, int BLK, bool SLOW>
+template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
-  using TS = emu::TileShape<TM, TN, WM, WN>;
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BLK, SLOW>;
+  using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G>;
   // the dynamic shared memory limit is a per-function, per-device attribute
   static bool configured[64] = {false};
   int dev = 0;
@@ -69,18 +75,22 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   return 0;
 }
 
-template <int TM, int TN, int WM, int WN>
+template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G = 1>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, 32, true>(p, st) : launch_one<TM, TN, WM, WN, 32, false>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G>(p, st);
   }
-  return slow ? launch_one<TM, TN, WM, WN, 16, true>(p, st) : launch_one<TM, TN, WM, WN, 16, false>(p, st);
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G>(p, st);
 }
 
-// Pick the tile with the lowest estimated time: waves of resident CTAs times the
-// work of one CTA, with a penalty when fewer than 8 warps per SM are in flight.
+// Pick the tile with the lowest estimated time per K element, in SM cycles: the
+// larger of the issue time of the CTAs an SM receives (128 lanes per clock) and
+// the latency-bound time of one thread's instruction stream (about one
+// instruction per two clocks when few warps share a scheduler).
 // EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
-int choose_tile(const emu::GemmParams& p) {
+int choose_tile(const emu::GemmParams& p, bool slow) {
   static int forced = -2;
   if (forced == -2) {
     forced = -1;
@@ -89,28 +99,35 @@ int choose_tile(const emu::GemmParams& p) {
       for (int t = 0; t < kNumTiles; ++t)
         if (std::strcmp(env, kTiles[t].name) == 0) forced = t;
   }
-  if (forced >= 0) return forced;
-  int best = 0;
+  auto usable = [&](int t) { return p.S == 1 || p.ktile % kTiles[t].bk == 0; };
+  if (forced >= 0 && usable(forced)) return forced;
+  int best = -1;
   double best_cost = 0.0;
   for (int t = 0; t < kNumTiles; ++t) {
-    const TileInfo& ti = kTiles[t];
+    if (!usable(t)) continue;
+    TileInfo ti = kTiles[t];
+    if (slow && t == 0) {                  // the large tile's slow variant needs 173 registers
+      ti.resident = 1;
+      ti.cost *= 1.1;
+    }
     const double ctas = (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
-    const double slots = (double)kSMs * ti.resident;
-    const double waves = std::ceil(ctas / slots);
-    const double warps_per_sm = std::min(ctas, slots) * (ti.threads / 32) / kSMs;
-    const double penalty = warps_per_sm < 8.0 ? 8.0 / warps_per_sm : 1.0;
-    const double est = waves * ti.bm * ti.bn * ti.cost * ti.resident * penalty;
-    if (t == 0 || est < best_cost) { best = t; best_cost = est; }
+    const double per_sm = std::ceil(ctas / kSMs);
+    const double t_issue = per_sm * ti.bm * ti.bn * ti.cost / 128.0;
+    const double t_latency = std::ceil(per_sm / ti.resident) * ti.tm * ti.tn * ti.cost * 2.0 / ti.g;
+    const double est = std::max(t_issue, t_latency);
+    if (best < 0 || est < best_cost) { best = t; best_cost = est; }
   }
   return best;
 }
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
-  switch (choose_tile(p)) {
-    case 0: return launch_tile<8, 4, 16, 16>(p, blk, slow, st);
-    case 1: return launch_tile<4, 2, 16, 20>(p, blk, slow, st);
-    case 2: return launch_tile<4, 4, 16, 8>(p, blk, slow, st);
-    default: return launch_tile<2, 2, 8, 16>(p, blk, slow, st);
+  switch (choose_tile(p, slow)) {
+    case 0: return launch_tile<8, 4, 16, 16, 32, false>(p, blk, slow, st);
+    case 1: return launch_tile<4, 2, 16, 20, 64, true>(p, blk, slow, st);
+    case 2: return launch_tile<4, 4, 16, 8, 32, false>(p, blk, slow, st);
+    case 3: return launch_tile<2, 2, 8, 16, 32, true>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 4, 32, false, 8>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 32, false, 4>(p, blk, slow, st);
   }
 }
 

@@ -123,15 +123,20 @@ __device__ __forceinline__ uint32_t c16_pair(float lo, float hi) {
 
 // ---------------------------------------------------------------------------
 // The GEMM kernel.  Thread tile TM x TN outputs; CTA WM x WN threads; K staged in
-// steps of BK = 32 codes through two shared-memory buffers (decode of stage s+1
-// overlaps nothing but needs only one barrier per stage); BLK products per block
-// (16 or 32); SLOW: restart chunks.
-template <int TM, int TN, int WM, int WN>
+// steps of BK_ (32 or 64) codes through two shared-memory buffers, so one barrier
+// per stage suffices; BLK products per block (16 or 32); SLOW: restart chunks;
+// DUAL: two partial sums per output in pass 2 (the terms are exact multiples of
+// 2^-149, so any association gives the same sum).  G > 1 ("lane split", for
+// skinny shapes with few, long chains): G adjacent lanes share one thread tile
+// and take every G-th product of each block; their partial block maxima and
+// partial sums are combined with warp shuffles (exact), so all G lanes hold the
+// same chain state.
+template <int TM, int TN, int WM, int WN, int BK_, int G = 1>
 struct TileShape {
-  static constexpr int NT = WM * WN;
+  static constexpr int NT = WM * WN * G;
   static constexpr int BM = WM * TM;
   static constexpr int BN = WN * TN;
-  static constexpr int BK = 32;
+  static constexpr int BK = BK_;
   // one stage buffer: A values [BK][BM] f32, A labels [BK][BM] u32 (label in both
   // halves), B values [BK][BN] f32, B labels [BK][BN] i16
   static constexpr int A_VAL = 0;
@@ -143,10 +148,12 @@ struct TileShape {
   static constexpr int SMEM_BYTES = 2 * STAGE_BYTES + LUT_BYTES;
 };
 
-template <int TM, int TN, int WM, int WN, int BLK, bool SLOW>
-__global__ void __launch_bounds__(WM * WN)
+template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G>
+__global__ void __launch_bounds__(WM * WN * G)
 emu_gemm_kernel(const GemmParams p) {
-  using TS = TileShape<TM, TN, WM, WN>;
+  using TS = TileShape<TM, TN, WM, WN, BK_, G>;
+  static_assert(G == 1 || G == 2 || G == 4 || G == 8, "lane groups of 1, 2, 4 or 8");
+  static_assert(BLK % G == 0, "a block's products are dealt evenly to the group");
   constexpr int NT = TS::NT;
   constexpr int BM = TS::BM;
   constexpr int BN = TS::BN;
@@ -163,7 +170,8 @@ emu_gemm_kernel(const GemmParams p) {
   uint2* lutB = lutA + 256;
 
   const int tid = threadIdx.x;
-  const int ty = tid / WN, tx = tid % WN;
+  const int gl = tid % G;                    // lane within the group
+  const int ty = (tid / G) / WN, tx = (tid / G) % WN;
   const int64_t m0 = (int64_t)blockIdx.y * BM;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int s = blockIdx.z;
@@ -179,7 +187,7 @@ emu_gemm_kernel(const GemmParams p) {
 
   // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
   const int64_t K = p.K;
-  const int kt = p.ktile;
+  const int kt = p.S == 1 ? BK : p.ktile;    // unsplit: any tiling of K is the same chain
   const int64_t T = (K + kt - 1) / kt;
   int64_t t_begin, t_end, t_stride;
   if (p.S == 1) { t_begin = 0; t_end = T; t_stride = 1; }
@@ -290,14 +298,16 @@ emu_gemm_kernel(const GemmParams p) {
 #pragma unroll
     for (int bb = 0; bb < NBLK; ++bb) {
       const int k0 = bb * BLK;
-      // ---- pass 1: block maximum of the label sums, started from |c'|
+      // ---- pass 1: block maximum of the product label sums (independent of the
+      //      chain state, so it can overlap the previous block), then with |c'|
       uint32_t E2[TM][TN / 2];
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int jp = 0; jp < TN / 2; ++jp) E2[i][jp] = c16_pair(cp[i][2 * jp], cp[i][2 * jp + 1]);
+        for (int jp = 0; jp < TN / 2; ++jp) E2[i][jp] = 0x80008000u;
 #pragma unroll
-      for (int kk = 0; kk < BLK; ++kk) {
+      for (int q = 0; q < BLK / G; ++q) {
+        const int kk = q * G + gl;
         uint32_t la[TM], lb[TN / 2];
 #pragma unroll
         for (int i = 0; i < TM; ++i) la[i] = sAl[(k0 + kk) * BM + ty * TM + i];
@@ -308,24 +318,38 @@ emu_gemm_kernel(const GemmParams p) {
 #pragma unroll
           for (int jp = 0; jp < TN / 2; ++jp) E2[i][jp] = __viaddmax_s16x2(la[i], lb[jp], E2[i][jp]);
       }
+      if (G > 1) {
+#pragma unroll
+        for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int jp = 0; jp < TN / 2; ++jp)
+              E2[i][jp] = __vmaxs2(E2[i][jp], __shfl_xor_sync(0xFFFFFFFFu, E2[i][jp], off));
+      }
       // ---- scales 2^(-43-E) (as fp32 bit patterns) and the running sums
       uint32_t sc[TM][TN];
-      float acc[TM][TN];
+      float acc[TM][TN], acc2[TM][TN];
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int jp = 0; jp < TN / 2; ++jp) {
-          const uint32_t e2 = __vmins2(E2[i][jp], kClampE2);
+          const uint32_t e2 = __vmins2(__vmaxs2(E2[i][jp], c16_pair(cp[i][2 * jp], cp[i][2 * jp + 1])),
+                                       kClampE2);
           sc[i][2 * jp] = kScaleBase - ((e2 << 16) & 0x7F800000u);
           sc[i][2 * jp + 1] = kScaleBase - (e2 & 0x7F800000u);
         }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fmul_rz(cp[i][j], __uint_as_float(sc[i][j]));
+        for (int j = 0; j < TN; ++j) {
+          acc[i][j] = (G == 1 || gl == 0) ? fmul_rz(cp[i][j], __uint_as_float(sc[i][j])) : 0.0f;
+          acc2[i][j] = 0.0f;
+        }
       // ---- pass 2: exact products, truncated onto the subnormal grid, summed exactly
 #pragma unroll
-      for (int kk = 0; kk < BLK; ++kk) {
+      for (int q = 0; q < BLK / G; ++q) {
+        const int kk = q * G + gl;
         float a[TM], b[TN];
 #pragma unroll
         for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ty * TM + i];
@@ -334,8 +358,26 @@ emu_gemm_kernel(const GemmParams p) {
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
-          for (int j = 0; j < TN; ++j)
-            acc[i][j] = fadd_rn(acc[i][j], fmul_rz(fmul_rn(a[i], b[j]), __uint_as_float(sc[i][j])));
+          for (int j = 0; j < TN; ++j) {
+            const float t = fmul_rz(fmul_rn(a[i], b[j]), __uint_as_float(sc[i][j]));
+            if (DUAL && (q & 1)) acc2[i][j] = fadd_rn(acc2[i][j], t);
+            else acc[i][j] = fadd_rn(acc[i][j], t);
+          }
+      }
+      if (DUAL) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) acc[i][j] = fadd_rn(acc[i][j], acc2[i][j]);
+      }
+      if (G > 1) {
+#pragma unroll
+        for (int off = 1; off < G; off <<= 1)
+#pragma unroll
+          for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+              acc[i][j] = fadd_rn(acc[i][j], __shfl_xor_sync(0xFFFFFFFFu, acc[i][j], off));
       }
       // ---- normalise: c' = S * 2^(E-13) * 2^-93, truncated to 14 significant bits
 #pragma unroll
@@ -376,6 +418,7 @@ emu_gemm_kernel(const GemmParams p) {
       else res[i][j] = fmul_rn(cp[i][j], kTwo93);
     }
 
+  if (G > 1 && gl != 0) return;             // the group's lanes hold the same results
   if (p.S > 1) {
     float* dst = p.partial + (int64_t)s * p.M * p.N;
 #pragma unroll

@@ -32,7 +32,9 @@ _SRC = os.path.join(_HERE, "emu_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 FORMATS = {"e4m3fn": 0, "e5m2": 1}
-OUT_DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+OUT_DTYPES = {"f32": 0, "bf16": 1, "f16": 2, "e4m3fn": 3, "e5m2": 4}
+OUT_NP = {"f32": np.uint32, "bf16": np.uint16, "f16": np.uint16, "e4m3fn": np.uint8,
+          "e5m2": np.uint8}
 
 #: instruction/platform presets: block width B, retained fraction bits F, slow
 #: restart R, c in alignment, split scheme (0 contiguous, 1 interleaved),
@@ -87,11 +89,12 @@ def lib() -> ctypes.CDLL:
         i32, i64, u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
         L.oracle_scaled_mm.argtypes = [P, ctypes.c_int, P, ctypes.c_int, i64, i64, i64, u32, u32,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.POINTER(Preset), P, ctypes.c_int]
+                                       ctypes.POINTER(Preset), P, ctypes.c_int, ctypes.c_int, u32]
         L.oracle_acc_sampled.argtypes = [P, ctypes.c_int, P, ctypes.c_int, i64, i64, i64,
                                          ctypes.c_int, ctypes.c_int, ctypes.POINTER(Preset),
                                          i64, P, P, P, ctypes.c_int]
-        L.oracle_epilogue.argtypes = [P, i64, u32, u32, ctypes.c_int, P]
+        L.oracle_epilogue.argtypes = [P, i64, u32, u32, ctypes.c_int, P, ctypes.c_int, u32]
+        L.oracle_f32_to_fp8.argtypes = [i64, P, ctypes.c_int, P]
         L.oracle_decode.argtypes = [ctypes.c_int, ctypes.c_int, P]
         L.oracle_products.argtypes = [i64, P, ctypes.c_int, P, ctypes.c_int, P]
         L.oracle_blk_many.argtypes = [i64, P, ctypes.c_int, P, ctypes.c_int, P, ctypes.c_int,
@@ -138,7 +141,7 @@ def _check(st: int, what: str):
 def scaled_mm(a_codes: np.ndarray, b_codes_nk: np.ndarray, fmt_a: str, fmt_b: str,
               scale_a: float, scale_b: float, out_dtype: str = "bf16",
               fast_accum: bool = True, split_S: int = 1, preset="hopper",
-              nthreads: int = 0) -> np.ndarray:
+              nthreads: int = 0, scale_result=None) -> np.ndarray:
     """Full GEMM.  ``a_codes`` [M,K] uint8 (row-major), ``b_codes_nk`` [N,K] uint8:
     the bytes of mat2 [K,N] column-major.  Returns the output bit patterns
     [M,N] (uint32 for f32, uint16 for bf16/f16)."""
@@ -147,12 +150,13 @@ def scaled_mm(a_codes: np.ndarray, b_codes_nk: np.ndarray, fmt_a: str, fmt_b: st
     M, K = a.shape
     N, K2 = b.shape
     assert K == K2
-    out = np.zeros((M, N), dtype=np.uint32 if out_dtype == "f32" else np.uint16)
+    out = np.zeros((M, N), dtype=OUT_NP[out_dtype])
     p = _preset(preset)
     st = lib().oracle_scaled_mm(_ptr(a), FORMATS[fmt_a], _ptr(b), FORMATS[fmt_b], M, N, K,
                                 _f32_bits(scale_a), _f32_bits(scale_b), OUT_DTYPES[out_dtype],
                                 int(bool(fast_accum)), int(split_S), ctypes.byref(p), _ptr(out),
-                                int(nthreads))
+                                int(nthreads), int(scale_result is not None),
+                                _f32_bits(1.0 if scale_result is None else scale_result))
     _check(st, "scaled_mm")
     return out
 
@@ -176,11 +180,13 @@ def acc_sampled(a_codes: np.ndarray, b_codes_nk: np.ndarray, fmt_a: str, fmt_b: 
     return out
 
 
-def epilogue(acc_bits: np.ndarray, scale_a: float, scale_b: float, out_dtype: str) -> np.ndarray:
+def epilogue(acc_bits: np.ndarray, scale_a: float, scale_b: float, out_dtype: str,
+             scale_result=None) -> np.ndarray:
     acc = np.ascontiguousarray(acc_bits, dtype=np.uint32)
-    out = np.zeros(acc.shape, dtype=np.uint32 if out_dtype == "f32" else np.uint16)
+    out = np.zeros(acc.shape, dtype=OUT_NP[out_dtype])
     st = lib().oracle_epilogue(_ptr(acc), acc.size, _f32_bits(scale_a), _f32_bits(scale_b),
-                               OUT_DTYPES[out_dtype], _ptr(out))
+                               OUT_DTYPES[out_dtype], _ptr(out), int(scale_result is not None),
+                               _f32_bits(1.0 if scale_result is None else scale_result))
     _check(st, "epilogue")
     return out
 
@@ -260,6 +266,14 @@ def f32_to_f16(a_bits):
     a = np.ascontiguousarray(a_bits, dtype=np.uint32)
     out = np.zeros(a.shape, dtype=np.uint16)
     lib().oracle_f32_to_f16(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def f32_to_fp8(a_bits, fmt: str) -> np.ndarray:
+    """fp32 -> FP8 codes, round to nearest even, saturating (NaN -> 0x7F)."""
+    a = np.ascontiguousarray(a_bits, dtype=np.uint32)
+    out = np.zeros(a.shape, dtype=np.uint8)
+    _check(lib().oracle_f32_to_fp8(a.size, _ptr(a), FORMATS[fmt], _ptr(out)), "f32_to_fp8")
     return out
 
 

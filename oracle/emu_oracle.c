@@ -43,7 +43,10 @@
  *    +Inf and -Inf together -> NaN, otherwise the Inf survives every later sum;
  *  - a contiguous split takes q = ceil(T/S) tiles, trailing splits may be empty;
  *  - the pairwise tree for general S adds p[i] += p[i + h], h = ceil(S/2);
- *  - canonical NaN is 0x7FC00000 (fp32), 0x7FC0 (bf16), 0x7E00 (fp16);
+ *  - canonical NaN is 0x7FC00000 (fp32), 0x7FC0 (bf16), 0x7E00 (fp16), 0x7F (fp8);
+ *  - fp8 output: z = RN32(y * scale_result) when scale_result is given (else
+ *    z = y), then round to nearest even into the format and saturate: finite
+ *    values and Inf beyond the largest finite code become +-max;
  *  - a block result beyond the fp32 range becomes +-Inf (unreachable at real K).
  *
  * The model uses no floating-point arithmetic: every value is an integer
@@ -65,6 +68,8 @@ typedef unsigned __int128 u128;
 #define OUT_F32 0
 #define OUT_BF16 1
 #define OUT_F16 2
+#define OUT_E4M3FN 3
+#define OUT_E5M2 4
 #define MODE_RNE 0
 #define MODE_RZ 1
 
@@ -264,6 +269,49 @@ static uint16_t f32_to_f16(uint32_t b) {
   if (v.cls == 2) return 0x7E00u;
   if (v.cls == 1) return (uint16_t)(0x7C00u | ((uint32_t)v.neg << 15));
   return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 11, -14, 15, 5, MODE_RNE);
+}
+
+/* fp32 -> FP8 (fmt 0 E4M3FN, 1 E5M2), round to nearest even, then saturate to the
+   format's largest finite value ("Validation evidence", claims table: fp8 outputs
+   saturate to the format's maximum); NaN -> 0x7F; +-Inf -> +-max; +-0 kept. */
+static uint8_t f32_to_fp8_sat(uint32_t b, int fmt) {
+  f32v v = f32_unpack(b);
+  const int fbits = fmt == FMT_E4M3FN ? 3 : 2;
+  const int bias = fmt == FMT_E4M3FN ? 7 : 15;
+  const int emin = 1 - bias;
+  /* largest finite: E4M3FN 1.110b * 2^8 = 14 * 2^5; E5M2 1.11b * 2^15 = 7 * 2^13 */
+  const u128 max_sig = fmt == FMT_E4M3FN ? 14 : 7;
+  const int max_exp2 = fmt == FMT_E4M3FN ? 5 : 13;
+  const uint8_t max_code = fmt == FMT_E4M3FN ? 0x7E : 0x7B;
+  const uint8_t sign = (uint8_t)(v.neg << 7);
+  if (v.cls == 2) return 0x7F;
+  if (v.cls == 1) return sign | max_code;
+  if (v.mag == 0) return sign;
+  /* round to nearest even on the format's grid, with no upper exponent limit */
+  u128 mag = v.mag;
+  int L = bitlen128(mag);
+  int lead = v.exp2 + L - 1;
+  int qe = lead - fbits;
+  if (qe < emin - fbits) qe = emin - fbits;
+  int shift = qe - v.exp2;
+  u128 q;
+  if (shift <= 0) {
+    q = mag << (-shift);
+  } else {
+    q = shift >= 128 ? 0 : (mag >> shift);
+    u128 rem = shift >= 128 ? mag : mag - (q << shift);
+    u128 half = shift > 128 ? 0 : ((u128)1 << (shift - 1));
+    if (shift <= 128 && (rem > half || (rem == half && (q & 1)))) q += 1;
+  }
+  if (q == ((u128)1 << (fbits + 1))) { q >>= 1; qe += 1; }
+  if (q == 0) return sign;
+  /* saturate: compare q * 2^qe with max_sig * 2^max_exp2 */
+  int cmp;
+  if (qe >= max_exp2) cmp = (qe - max_exp2 > 60) || ((q << (qe - max_exp2)) > max_sig);
+  else cmp = (max_exp2 - qe <= 60) && (q > (max_sig << (max_exp2 - qe)));
+  if (cmp) return sign | max_code;
+  if (q < ((u128)1 << fbits)) return sign | (uint8_t)q;            /* subnormal */
+  return sign | (uint8_t)(((qe + fbits + bias) << fbits) | (int)(q - ((u128)1 << fbits)));
 }
 
 /* ------------------------------------------------------------------------- */
@@ -468,9 +516,16 @@ static uint32_t acc_one(const gemm_t* g, int64_t m, int64_t n, scratch_t* w) {
 }
 
 /* epilogue [LIM-C; VAL-H]: alpha = RN32(sa*sb); y = fma(acc, alpha, +0);
-   bf16/fp16 rounded from y; NaN outputs canonical */
-static void epilogue_store(uint32_t acc, uint32_t alpha, int out_dtype, void* out, int64_t i) {
+   bf16/fp16 rounded from y; fp8: a separate fp32 multiply by scale_result, then
+   saturating conversion; NaN outputs canonical */
+static void epilogue_store(uint32_t acc, uint32_t alpha, int out_dtype, int has_sr,
+                           uint32_t sr, void* out, int64_t i) {
   uint32_t y = f32_fma_plus0(acc, alpha);
+  if (out_dtype == OUT_E4M3FN || out_dtype == OUT_E5M2) {
+    uint32_t z = has_sr ? f32_mul_rn(y, sr) : y;
+    ((uint8_t*)out)[i] = f32_to_fp8_sat(z, out_dtype == OUT_E4M3FN ? FMT_E4M3FN : FMT_E5M2);
+    return;
+  }
   if (out_dtype == OUT_F32) {
     f32v v = f32_unpack(y);
     ((uint32_t*)out)[i] = (v.cls == 2) ? F32_CANON_NAN : y;
@@ -564,10 +619,10 @@ static int run_jobs(const gemm_t* g, const int64_t* im, const int64_t* in, int64
 int oracle_scaled_mm(const uint8_t* A, int fmt_a, const uint8_t* B, int fmt_b,
                      int64_t M, int64_t N, int64_t K, uint32_t scale_a_bits, uint32_t scale_b_bits,
                      int out_dtype, int fast_accum, int split_S, const orc_preset_t* preset,
-                     void* out, int nthreads) {
+                     void* out, int nthreads, int has_scale_result, uint32_t scale_result_bits) {
   int st = check_args(fmt_a, fmt_b, M, N, K, split_S, preset);
   if (st) return st;
-  if (out_dtype < 0 || out_dtype > 2) return ORC_EINVAL;
+  if (out_dtype < 0 || out_dtype > 4) return ORC_EINVAL;
   int64_t count = M * N;
   if (count == 0) return ORC_OK;
   gemm_t* g = (gemm_t*)malloc(sizeof(gemm_t));
@@ -577,7 +632,8 @@ int oracle_scaled_mm(const uint8_t* A, int fmt_a, const uint8_t* B, int fmt_b,
   st = run_jobs(g, NULL, NULL, count, acc, nthreads);
   if (st == ORC_OK) {
     uint32_t alpha = f32_mul_rn(scale_a_bits, scale_b_bits);
-    for (int64_t i = 0; i < count; ++i) epilogue_store(acc[i], alpha, out_dtype, out, i);
+    for (int64_t i = 0; i < count; ++i)
+      epilogue_store(acc[i], alpha, out_dtype, has_scale_result, scale_result_bits, out, i);
   }
   free(g); free(acc);
   return st;
@@ -603,10 +659,19 @@ int oracle_acc_sampled(const uint8_t* A, int fmt_a, const uint8_t* B, int fmt_b,
 
 /* the epilogue alone over a vector of accumulators */
 int oracle_epilogue(const uint32_t* acc, int64_t count, uint32_t scale_a_bits,
-                    uint32_t scale_b_bits, int out_dtype, void* out) {
-  if (out_dtype < 0 || out_dtype > 2 || count < 0) return ORC_EINVAL;
+                    uint32_t scale_b_bits, int out_dtype, void* out, int has_scale_result,
+                    uint32_t scale_result_bits) {
+  if (out_dtype < 0 || out_dtype > 4 || count < 0) return ORC_EINVAL;
   uint32_t alpha = f32_mul_rn(scale_a_bits, scale_b_bits);
-  for (int64_t i = 0; i < count; ++i) epilogue_store(acc[i], alpha, out_dtype, out, i);
+  for (int64_t i = 0; i < count; ++i)
+    epilogue_store(acc[i], alpha, out_dtype, has_scale_result, scale_result_bits, out, i);
+  return ORC_OK;
+}
+
+/* fp32 -> FP8 with saturation over a vector (fmt 0 E4M3FN, 1 E5M2) */
+int oracle_f32_to_fp8(int64_t n, const uint32_t* a, int fmt, uint8_t* out) {
+  if (fmt < 0 || fmt > 1) return ORC_EINVAL;
+  for (int64_t i = 0; i < n; ++i) out[i] = f32_to_fp8_sat(a[i], fmt);
   return ORC_OK;
 }
 

@@ -199,7 +199,7 @@ def accumulator(a_row, b_col, fmt_a, fmt_b, fast=True, S=1, preset="hopper",
     return combine(parts, pairwise)
 
 
-def epilogue(acc, scale_a: float, scale_b: float, out_dtype: str) -> int:
+def epilogue(acc, scale_a: float, scale_b: float, out_dtype: str, scale_result=None) -> int:
     """alpha = RN32(sa*sb); y = fma(acc, alpha, +0); bf16/fp16 rounded from y;
     NaN canonical (0x7FC00000 / 0x7FC0 / 0x7E00).  Returns output bits."""
     import torch  # fp32 -> bf16 rounding by the library cast
@@ -211,6 +211,17 @@ def epilogue(acc, scale_a: float, scale_b: float, out_dtype: str) -> int:
     else:
         prod = float(acc) * float(alpha)          # exact in binary64
         y = np.float32(0.0) if prod == 0 else np.float32(prod)  # one rounding
+    if out_dtype in ("e4m3fn", "e5m2"):
+        # a separate fp32 multiply by scale_result, then round-to-nearest-even into
+        # the format with saturation to its maximum: the clamp before torch's cast
+        # gives the same code as rounding first and saturating after
+        z = y if scale_result is None else np.float32(y) * np.float32(scale_result)
+        if np.isnan(z):
+            return 0x7F
+        mx = 448.0 if out_dtype == "e4m3fn" else 57344.0
+        zt = torch.tensor([float(z)], dtype=torch.float32).clamp(-mx, mx)
+        dt = torch.float8_e4m3fn if out_dtype == "e4m3fn" else torch.float8_e5m2
+        return int(zt.to(dt).view(torch.uint8).item())
     if out_dtype == "f32":
         if np.isnan(y):
             return 0x7FC00000

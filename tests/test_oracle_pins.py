@@ -593,3 +593,46 @@ def test_round_helper_vs_numpy(orc):
             want16 = int(np.array([-v if neg else v], np.float64).astype(np.float16).view(np.uint16)[0])
         assert orc.round_bits(neg, mag, exp2, 0, 0) == want32
         assert orc.round_bits(neg, mag, exp2, 2, 0) == want16
+
+
+# fp8 output ("Validation evidence", claims table: scale_result is a separate fp32
+# multiply before saturation to the format's maximum): round to nearest even into
+# the format, saturate to +-max (Inf too), NaN -> 0x7F.  Against torch's fp8 cast
+# of the value clamped to +-max (which rounds to nearest even).
+@pytest.mark.parametrize("fmt", FMTS)
+def test_f32_to_fp8_saturating_vs_torch(orc, fmt):
+    rng = np.random.default_rng(22)
+    mx = 448.0 if fmt == "e4m3fn" else 57344.0
+    x = _special_f32(rng, 300000)
+    # values near the format's range: ties, midpoints, near max and subnormals
+    near = (rng.normal(size=100000) * mx * np.exp2(rng.integers(-20, 3, 100000))).astype(np.float32)
+    codes = np.arange(256, dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(TORCH_FP8[fmt]).to(torch.float32).numpy()
+    vals = vals[np.isfinite(vals)]
+    mids = ((vals[:, None] + vals[None, :]) / 2).astype(np.float32).ravel()
+    x = np.concatenate([x, bits32(near), bits32(mids), bits32(vals)])
+    got = orc.f32_to_fp8(x, fmt)
+    xf = torch.from_numpy(f32(x).copy()).clamp(-mx, mx)
+    want = xf.to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+    want = np.where(np.isnan(f32(x)), np.uint8(0x7F), want)
+    assert np.array_equal(got, want), np.flatnonzero(got != want)[:10]
+
+
+def test_fp8_output_epilogue_rounds_scale_result_separately(orc):
+    rng = np.random.default_rng(23)
+    acc = (rng.normal(size=50000) * np.exp2(rng.integers(-10, 20, 50000))).astype(np.float32)
+    for sa, sb, sr in ((1 / 64, 1 / 32, 3.0), (0.7, 1.3, 0.11), (1.0, 1.0, 1e-30), (2.0, 3.0, -5.0)):
+        for fmt in FMTS:
+            got = orc.epilogue(bits32(acc), sa, sb, fmt, scale_result=sr)
+            alpha = np.float32(sa) * np.float32(sb)
+            prod = acc.astype(np.float64) * np.float64(alpha)
+            y = np.where(prod == 0, np.float32(0.0), prod.astype(np.float32))
+            z = (y * np.float32(sr)).astype(np.float32)              # separate fp32 multiply
+            mx = 448.0 if fmt == "e4m3fn" else 57344.0
+            want = torch.from_numpy(z.copy()).clamp(-mx, mx).to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+            want = np.where(np.isnan(z), np.uint8(0x7F), want)
+            assert np.array_equal(got, want), (sa, sb, sr, fmt)
+    # without scale_result: the fp32 y converts directly
+    got = orc.epilogue(bits32(acc), 1.0, 1.0, "e4m3fn")
+    want = torch.from_numpy(acc.copy()).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)

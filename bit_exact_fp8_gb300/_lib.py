@@ -20,10 +20,13 @@ EMU_E5M2 = 1
 EMU_OUT_F32 = 0
 EMU_OUT_BF16 = 1
 EMU_OUT_F16 = 2
+EMU_OUT_E4M3FN = 3
+EMU_OUT_E5M2 = 4
 
 #: every symbol include/emu_fp8.h declares
 EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
-            "emu_abi_version", "emu_scaled_mm_noalloc")
+            "emu_abi_version", "emu_scaled_mm_noalloc", "emu_device_status",
+            "emu_selftest_wait_timeout", "emu_scaled_mm_ex")
 
 #: size of the static scratch of emu_scaled_mm_noalloc (EMU_NOALLOC_SCRATCH_BYTES)
 EMU_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -60,11 +63,20 @@ def load(path: str = LIB) -> ctypes.CDLL:
                                 ctypes.c_int64, P, P, P, ctypes.c_int, ctypes.c_int32,
                                 ctypes.c_int32, ctypes.POINTER(emu_preset_t), P, ctypes.c_size_t, P]
     L.emu_scaled_mm.restype = ctypes.c_int
+    L.emu_scaled_mm_ex.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int64,
+                                   ctypes.c_int64, ctypes.c_int64, P, P, P, P, ctypes.c_int,
+                                   ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(emu_preset_t),
+                                   P, ctypes.c_size_t, P]
+    L.emu_scaled_mm_ex.restype = ctypes.c_int
     L.emu_scaled_mm_noalloc.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int64, P, P, P, ctypes.c_int,
                                         ctypes.c_int32, ctypes.c_int32,
                                         ctypes.POINTER(emu_preset_t), P]
     L.emu_scaled_mm_noalloc.restype = ctypes.c_int
+    L.emu_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
+    L.emu_device_status.restype = ctypes.c_int
+    L.emu_selftest_wait_timeout.argtypes = [P]
+    L.emu_selftest_wait_timeout.restype = ctypes.c_int
     L.emu_last_error.argtypes = []
     L.emu_last_error.restype = ctypes.c_char_p
     L.emu_abi_version.argtypes = []
@@ -114,3 +126,28 @@ def emu_scaled_mm_noalloc(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int
         ctypes.c_void_p(A), fmt_a, ctypes.c_void_p(B), fmt_b, M, N, K,
         ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(out), out_dtype,
         int(fast_accum), int(split_S), ctypes.byref(preset), ctypes.c_void_p(stream)))
+
+
+def emu_device_status(reset: bool = False) -> int:
+    """The library's device status word (0 ok, 1 a bounded wait gave up); synchronous."""
+    v = ctypes.c_int32(0)
+    st = load().emu_device_status(ctypes.byref(v), int(bool(reset)))
+    if st != EMU_OK:
+        raise RuntimeError(f"emu_device_status failed: {emu_last_error()}")
+    return int(v.value)
+
+
+def emu_selftest_wait_timeout(stream: int = 0) -> int:
+    return int(load().emu_selftest_wait_timeout(ctypes.c_void_p(stream)))
+
+
+def emu_scaled_mm_ex(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int, K: int,
+                     scale_a: int, scale_b: int, scale_result: int, out: int, out_dtype: int,
+                     fast_accum: int, split_S: int, preset: emu_preset_t, workspace: int,
+                     workspace_bytes: int, stream: int) -> int:
+    """emu_scaled_mm with scale_result (0: none) for FP8 outputs; returns the status."""
+    return int(load().emu_scaled_mm_ex(
+        ctypes.c_void_p(A), fmt_a, ctypes.c_void_p(B), fmt_b, M, N, K,
+        ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(scale_result or None),
+        ctypes.c_void_p(out), out_dtype, int(fast_accum), int(split_S), ctypes.byref(preset),
+        ctypes.c_void_p(workspace), int(workspace_bytes), ctypes.c_void_p(stream)))

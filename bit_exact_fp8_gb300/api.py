@@ -15,7 +15,8 @@ from . import _lib
 
 _FMT = {torch.float8_e4m3fn: _lib.EMU_E4M3FN, torch.float8_e5m2: _lib.EMU_E5M2}
 _OUT = {torch.float32: _lib.EMU_OUT_F32, torch.bfloat16: _lib.EMU_OUT_BF16,
-        torch.float16: _lib.EMU_OUT_F16}
+        torch.float16: _lib.EMU_OUT_F16, torch.float8_e4m3fn: _lib.EMU_OUT_E4M3FN,
+        torch.float8_e5m2: _lib.EMU_OUT_E5M2}
 
 
 class EmuError(Exception):
@@ -28,8 +29,8 @@ class ReferenceRejectsError(EmuError, RuntimeError):
 
 
 class UnsupportedFeatureError(EmuError, NotImplementedError):
-    """bias, row-wise scales, fp8 output, grad mode, or a preset the kernels do
-    not implement ("Limitations of mmaemu v0.1", table "Features outside v0.1")."""
+    """bias, row-wise scales, grad mode, or a preset the kernels do not
+    implement ("Limitations of mmaemu v0.1", table "Features outside v0.1")."""
 
 
 class EmuCudaError(EmuError, RuntimeError):
@@ -71,11 +72,9 @@ def scaled_mm(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
     device, scale_a/scale_b one-element fp32 tensors there.  ``splitk`` is the
     explicit split-K factor S, ``preset`` "hopper" (default) or "ada" or a
     parameter dict.  Returns out [M,N] (out_dtype defaults to mat1's dtype, as in
-    torch; an FP8 out_dtype is not modelled here and raises)."""
+    torch; an FP8 out_dtype takes the optional one-element ``scale_result``)."""
     if bias is not None:
         raise UnsupportedFeatureError("bias is not supported (it raises on the reference too)")
-    if scale_result is not None:
-        raise UnsupportedFeatureError("scale_result (fp8 output) is not supported")
     if torch.is_grad_enabled() and any(t.requires_grad for t in (mat1, mat2)):
         raise UnsupportedFeatureError("inference only: inputs require grad under grad mode")
     if mat1.dim() != 2 or mat2.dim() != 2:
@@ -95,6 +94,10 @@ def scaled_mm(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
         raise ReferenceRejectsError("mat1 must be row-major")
     if mat2.numel() > 0 and not (mat2.stride(0) == 1 and (mat2.stride(1) == K or N <= 1)):
         raise ReferenceRejectsError("mat2 must be column-major ([K, N] with K contiguous, e.g. w.t())")
+    if scale_result is not None and (not scale_result.is_cuda or scale_result.device != dev
+                                     or scale_result.numel() != 1
+                                     or scale_result.dtype != torch.float32):
+        raise ValueError("scale_result must be a one-element float32 tensor on the device")
     for name, sc in (("scale_a", scale_a), ("scale_b", scale_b)):
         if sc.numel() != 1:
             raise UnsupportedFeatureError(f"row-wise {name} is not supported (tensor-wise only)")
@@ -115,10 +118,11 @@ def scaled_mm(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
     ws_ptr = workspace.data_ptr() if (workspace is not None and need > 0) else 0
     ws_bytes = workspace.numel() * workspace.element_size() if (workspace is not None and need > 0) else 0
     stream = torch.cuda.current_stream(dev).cuda_stream
-    st = _lib.emu_scaled_mm(mat1.data_ptr(), _FMT[mat1.dtype], mat2.data_ptr(), _FMT[mat2.dtype],
-                            M, N, K, scale_a.data_ptr(), scale_b.data_ptr(), out.data_ptr(),
-                            _OUT[out_dtype], int(bool(use_fast_accum)), int(splitk), P,
-                            ws_ptr, ws_bytes, stream)
+    sr_ptr = scale_result.data_ptr() if scale_result is not None else 0
+    st = _lib.emu_scaled_mm_ex(mat1.data_ptr(), _FMT[mat1.dtype], mat2.data_ptr(),
+                               _FMT[mat2.dtype], M, N, K, scale_a.data_ptr(), scale_b.data_ptr(),
+                               sr_ptr, out.data_ptr(), _OUT[out_dtype], int(bool(use_fast_accum)),
+                               int(splitk), P, ws_ptr, ws_bytes, stream)
     if st != _lib.EMU_OK:
         _raise(st, "emu_scaled_mm")
     return out

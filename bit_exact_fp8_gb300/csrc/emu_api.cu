@@ -6,6 +6,8 @@
 #include "emu_fp8.h"
 #include "emu_kernels.cuh"
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
@@ -37,8 +39,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 //   M40  4 x 2, 16 x 20 threads, BK 64:  64 x 40 (M <= 64 with wide N: one CTA per SM)
 //   M32  4 x 4, 16 x  8 threads, BK 32:  64 x 32
 //   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32 (skinny, split-K)
-//   K8   1 x 2,  4 x  4 x 8 lanes, BK 32:  4 x  8, each block split over 8 lanes
-//   K4   1 x 2,  4 x  8 x 4 lanes, BK 32:  4 x 16, each block split over 4 lanes
+//   K8   1 x 2,  4 x  4 x 8 lanes, BK 64:  4 x  8, each block split over 8 lanes
+//   K4   1 x 2,  4 x  8 x 4 lanes, BK 64:  4 x 16, each block split over 4 lanes
 //        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
 //        CTA tile must stay tiny for every SM to get work)
 struct TileInfo {
@@ -51,11 +53,43 @@ constexpr TileInfo kTiles[] = {
     {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15},
     {"M32", 4, 4, 64, 32, 128, 3, 32, 1, 1.05},
     {"S", 2, 2, 16, 32, 128, 4, 32, 1, 1.50},
-    {"K8", 1, 2, 4, 8, 128, 8, 32, 8, 3.00},
-    {"K4", 1, 2, 4, 16, 128, 8, 32, 4, 2.40},
+    {"K8", 1, 2, 4, 8, 128, 8, 64, 8, 3.00},
+    {"K4", 1, 2, 4, 16, 128, 8, 64, 4, 2.40},
 };
 constexpr int kNumTiles = 6;
 constexpr int kSMs = 152;
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D u8 tensor map of a K-contiguous operand [rows, K] with box [box_rows, box_k]
+int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K,
+                     int box_rows, int box_k) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(EMU_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
+  const cuuint32_t elem[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
+                         strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(EMU_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return EMU_OK;
+}
 
 template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
@@ -69,10 +103,15 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM_BYTES);
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
+  CUtensorMap tmA, tmB;
+  int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK);
+  if (rc != EMU_OK) return rc;
+  rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK);
+  if (rc != EMU_OK) return rc;
   dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)((p.M + TS::BM - 1) / TS::BM),
             (unsigned)p.S);
-  kern<<<grid, TS::NT, TS::SMEM_BYTES, st>>>(p);
-  return 0;
+  kern<<<grid, TS::NT, TS::SMEM_BYTES, st>>>(p, tmA, tmB);
+  return EMU_OK;
 }
 
 template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G = 1>
@@ -126,8 +165,8 @@ int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
     case 1: return launch_tile<4, 2, 16, 20, 64, true>(p, blk, slow, st);
     case 2: return launch_tile<4, 4, 16, 8, 32, false>(p, blk, slow, st);
     case 3: return launch_tile<2, 2, 8, 16, 32, true>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 4, 32, false, 8>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 32, false, 4>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 4, 64, false, 8>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 64, false, 4>(p, blk, slow, st);
   }
 }
 
@@ -199,12 +238,26 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t
                   void* out, emu_out_t out_dtype, int32_t fast_accum, int32_t split_S,
                   const emu_preset_t* preset, void* workspace, size_t workspace_bytes,
                   void* stream) {
+  return emu_scaled_mm_ex(A, fmt_a, B, fmt_b, M, N, K, scale_a, scale_b, nullptr, out, out_dtype,
+                          fast_accum, split_S, preset, workspace, workspace_bytes, stream);
+}
+
+int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,
+                     int64_t M, int64_t N, int64_t K, const float* scale_a, const float* scale_b,
+                     const float* scale_result, void* out, emu_out_t out_dtype,
+                     int32_t fast_accum, int32_t split_S, const emu_preset_t* preset,
+                     void* workspace, size_t workspace_bytes, void* stream) {
   g_last_error.clear();
   if (!preset) return fail(EMU_EINVAL, "preset is null");
   if ((int)fmt_a < 0 || (int)fmt_a > 1 || (int)fmt_b < 0 || (int)fmt_b > 1)
     return fail(EMU_EINVAL, "unknown FP8 format (%d, %d)", (int)fmt_a, (int)fmt_b);
-  if ((int)out_dtype < 0 || (int)out_dtype > 2)
+  if ((int)out_dtype < 0 || (int)out_dtype > 4)
     return fail(EMU_EINVAL, "unknown output dtype %d", (int)out_dtype);
+  const bool fp8_out = out_dtype == EMU_OUT_E4M3FN || out_dtype == EMU_OUT_E5M2;
+  if (scale_result && !fp8_out)
+    return fail(EMU_EUNSUPPORTED, "scale_result applies to fp8 outputs only");
+  if (fmt_a == EMU_E4M3FN && fmt_b == EMU_E4M3FN && out_dtype == EMU_OUT_E5M2)
+    return fail(EMU_EREJECT, "cuBLASLt refuses e4m3 x e4m3 -> e5m2");
   if (M < 0 || N < 0 || K < 0) return fail(EMU_EINVAL, "negative size (%lld, %lld, %lld)",
                                            (long long)M, (long long)N, (long long)K);
   if (split_S < 1) return fail(EMU_EINVAL, "split_S must be >= 1 (got %d)", split_S);
@@ -249,6 +302,7 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t
   p.fmt_a = (int)fmt_a; p.fmt_b = (int)fmt_b;
   p.scale_a = scale_a; p.scale_b = scale_b;
   p.out = out; p.out_dtype = (int)out_dtype;
+  p.scale_result = scale_result;
   p.partial = static_cast<float*>(workspace);
   p.S = split_S; p.scheme = preset->split_scheme; p.ktile = preset->ktile;
   p.restart_blocks = preset->restart / preset->block_width;
@@ -261,7 +315,8 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t
     const int64_t blocks = (MN + threads - 1) / threads;
     emu::emu_fill_k0_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(p);
   } else {
-    launch_gemm(p, preset->block_width, fast_accum == 0, st);
+    const int rc = launch_gemm(p, preset->block_width, fast_accum == 0, st);
+    if (rc != EMU_OK) return rc;
     if (split_S > 1) {
       const int64_t MN = M * N;
       const int threads = 256;
@@ -296,6 +351,31 @@ int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, e
   }
   return emu_scaled_mm(A, fmt_a, B, fmt_b, M, N, K, scale_a, scale_b, out, out_dtype, fast_accum,
                        split_S, preset, ws, ws_bytes, stream);
+}
+
+int emu_device_status(int32_t* status, int32_t reset) {
+  if (!status) return fail(EMU_EINVAL, "status is null");
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, emu::g_emu_device_status, sizeof v);
+  if (e != cudaSuccess) return fail(EMU_ECUDA, "reading the device status failed: %s",
+                                    cudaGetErrorString(e));
+  *status = v;
+  if (reset) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(emu::g_emu_device_status, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(EMU_ECUDA, "clearing the device status failed: %s",
+                                      cudaGetErrorString(e));
+  }
+  return EMU_OK;
+}
+
+int emu_selftest_wait_timeout(void* stream) {
+  g_last_error.clear();
+  cudaGetLastError();
+  emu::emu_wait_timeout_selftest_kernel<<<1, 64, 0, static_cast<cudaStream_t>(stream)>>>(64u);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(EMU_ECUDA, "CUDA launch failed: %s", cudaGetErrorString(e));
+  return EMU_OK;
 }
 
 }  // extern "C"

@@ -38,8 +38,18 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>          // CUtensorMap (the type only; the library calls the driver via an entry point)
 
 namespace emu {
+
+// Device status word of the library: 0, or kStatusWaitTimeout after a pipeline wait
+// gave up (the affected CTA returns early; its outputs are not valid).
+constexpr int kStatusWaitTimeout = 1;
+__device__ int g_emu_device_status = 0;
+
+// mbarrier.try_wait polls before a wait gives up.  Each poll suspends the thread
+// for a short, hardware-defined time, so this bounds a wait to well under seconds.
+constexpr uint32_t kWaitPolls = 1u << 20;
 
 constexpr int kPreA = 46;             // A values carry 2^-46
 constexpr int kPreB = 47;             // B values carry 2^-47 (x' = x * 2^-93)
@@ -59,7 +69,8 @@ struct GemmParams {
   const float* scale_a;
   const float* scale_b;
   void* out;               // [M,N] row-major
-  int out_dtype;           // 0 f32, 1 bf16, 2 f16
+  int out_dtype;           // 0 f32, 1 bf16, 2 f16, 3 e4m3fn, 4 e5m2
+  const float* scale_result;  // fp8 outputs: optional fp32 multiplier applied after alpha
   float* partial;          // [S,M,N] fp32 split partials (S > 1)
   int S;                   // split factor
   int scheme;              // 0 contiguous tiles, 1 round-robin tiles
@@ -90,6 +101,89 @@ __device__ __forceinline__ float fma_plus0(float a, float b) {
   asm("fma.rn.f32 %0, %1, %2, 0f00000000;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+
+// ---------------------------------------------------------------------------
+// TMA + mbarrier helpers (inline PTX, sm_90+)
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, P;\n}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0u;
+}
+// wait for the phase with this parity to complete; false if it gave up
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// Output stores.  fp32: y; bf16/fp16: rounded to nearest even from y; fp8: a
+// separate fp32 multiply by scale_result (when given), then round to nearest even
+// into the format with saturation to its largest finite value ("Validation
+// evidence", claims table, fp8-output row).  NaN outputs are canonical.
+__device__ __forceinline__ uint32_t f32_to_fp8_satfinite(float z, int out_dtype) {
+  uint16_t r;
+  if (out_dtype == 3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(z));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(z));
+  return r & 0xFFu;                        // the second source lands in the low byte
+}
+
+struct OutStore {
+  bool has_sr;
+  float sr;
+  __device__ __forceinline__ explicit OutStore(const GemmParams& p)
+      : has_sr(p.scale_result != nullptr), sr(p.scale_result ? __ldg(p.scale_result) : 1.0f) {}
+  __device__ __forceinline__ void operator()(const GemmParams& p, int64_t i, float y) const {
+    const bool nan_y = (__float_as_uint(y) & 0x7FFFFFFFu) > 0x7F800000u;
+    if (p.out_dtype == 0) {
+      reinterpret_cast<uint32_t*>(p.out)[i] = nan_y ? 0x7FC00000u : __float_as_uint(y);
+    } else if (p.out_dtype == 1) {
+      const __nv_bfloat16 h = __float2bfloat16_rn(y);
+      reinterpret_cast<uint16_t*>(p.out)[i] =
+          nan_y ? (uint16_t)0x7FC0u : *reinterpret_cast<const uint16_t*>(&h);
+    } else if (p.out_dtype == 2) {
+      const __half h = __float2half_rn(y);
+      reinterpret_cast<uint16_t*>(p.out)[i] =
+          nan_y ? (uint16_t)0x7E00u : *reinterpret_cast<const uint16_t*>(&h);
+    } else {
+      const float z = has_sr ? fmul_rn(y, sr) : y;
+      const bool nan_z = (__float_as_uint(z) & 0x7FFFFFFFu) > 0x7F800000u;
+      reinterpret_cast<uint8_t*>(p.out)[i] =
+          nan_z ? (uint8_t)0x7Fu : (uint8_t)f32_to_fp8_satfinite(z, p.out_dtype);
+    }
+  }
+};
 
 // decode one FP8 code into the pre-scaled fp32 value and the 16-bit label
 __device__ __forceinline__ void decode_code(uint32_t code, int fmt, int pre, float& v, int& lab) {
@@ -144,13 +238,23 @@ struct TileShape {
   static constexpr int B_VAL = A_LAB + BK * BM * 4;
   static constexpr int B_LAB = B_VAL + BK * BN * 4;
   static constexpr int STAGE_BYTES = ((B_LAB + BK * BN * 2) + 127) / 128 * 128;
+  // ring of raw FP8 boxes filled by TMA: A [BM][BK] then B [BN][BK] bytes per slot
+  static constexpr int RAW_A = BM * BK;
+  static constexpr int RAW_B = BN * BK;
+  static constexpr int RAW_STAGE = ((RAW_A + RAW_B) + 127) / 128 * 128;
+  static constexpr int NS = RAW_STAGE <= 1024 ? 8 : (BM >= 128 ? 3 : 4);   // ring depth
+  static constexpr int RAW_OFF = 2 * STAGE_BYTES;
   static constexpr int LUT_BYTES = 2 * 256 * 8;
-  static constexpr int SMEM_BYTES = 2 * STAGE_BYTES + LUT_BYTES;
+  static constexpr int LUT_OFF = RAW_OFF + NS * RAW_STAGE;
+  static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8;
+  static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
 };
 
 template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G>
 __global__ void __launch_bounds__(WM * WN * G)
-emu_gemm_kernel(const GemmParams p) {
+emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB) {
   using TS = TileShape<TM, TN, WM, WN, BK_, G>;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "lane groups of 1, 2, 4 or 8");
   static_assert(BLK % G == 0, "a block's products are dealt evenly to the group");
@@ -163,11 +267,13 @@ emu_gemm_kernel(const GemmParams p) {
   constexpr int B_CHUNKS = BN * BK / 16;
   constexpr int A_PER = (A_CHUNKS + NT - 1) / NT;
   constexpr int B_PER = (B_CHUNKS + NT - 1) / NT;
+  constexpr int NS = TS::NS;
   static_assert(TN % 2 == 0, "labels are paired along N");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  uint2* lutA = reinterpret_cast<uint2*>(smem + 2 * TS::STAGE_BYTES);
+  uint2* lutA = reinterpret_cast<uint2*>(smem + TS::LUT_OFF);
   uint2* lutB = lutA + 256;
+  const uint32_t bar0 = smem_u32(smem + TS::BAR_OFF);
 
   const int tid = threadIdx.x;
   const int gl = tid % G;                    // lane within the group
@@ -207,36 +313,24 @@ emu_gemm_kernel(const GemmParams p) {
     n_stages -= stages_per_tile - (len_last + BK - 1) / BK;
   }
 
-  uint4 ra[A_PER], rb[B_PER];
-  auto load_stage = [&](int64_t st) {
+  auto stage_k = [&](int64_t st) -> int {
     const int64_t tl = st / stages_per_tile;
-    const int64_t k = (t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK;
-    const int64_t rem = K - k;
-    const int valid = rem < BK ? (int)rem : BK;
-#pragma unroll
-    for (int r = 0; r < A_PER; ++r) {
-      const int c = tid + r * NT;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (c < A_CHUNKS) {
-        const int row = c / (BK / 16), h = c % (BK / 16);
-        if (m0 + row < p.M && h * 16 < valid)
-          v = __ldg(reinterpret_cast<const uint4*>(p.A + (m0 + row) * K + k + h * 16));
-      }
-      ra[r] = v;
-    }
-#pragma unroll
-    for (int r = 0; r < B_PER; ++r) {
-      const int c = tid + r * NT;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (c < B_CHUNKS) {
-        const int col = c / (BK / 16), h = c % (BK / 16);
-        if (n0 + col < p.N && h * 16 < valid)
-          v = __ldg(reinterpret_cast<const uint4*>(p.B + (n0 + col) * K + k + h * 16));
-      }
-      rb[r] = v;
-    }
+    return (int)((t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK);
   };
-  auto store_stage = [&](int buf) {
+  // one thread: start the TMA loads of stage st into its ring slot.  Boxes reaching
+  // past M, N or K are zero-filled, and zero codes are neutral in every block.
+  auto issue = [&](int64_t st) {
+    const int slot = (int)(st % NS);
+    const uint32_t bar = bar0 + 8u * slot;
+    const uint32_t dst = smem_u32(smem + TS::RAW_OFF + slot * TS::RAW_STAGE);
+    const int k = stage_k(st);
+    mbar_arrive_expect_tx(bar, (uint32_t)(TS::RAW_A + TS::RAW_B));
+    tma_load_2d(dst, &tmA, k, (int)m0, bar);
+    tma_load_2d(dst + TS::RAW_A, &tmB, k, (int)n0, bar);
+  };
+  // all threads: decode the raw slot of stage st into operand buffer buf
+  auto decode_stage = [&](int64_t st, int buf) {
+    const unsigned char* raw = smem + TS::RAW_OFF + (int)(st % NS) * TS::RAW_STAGE;
     unsigned char* base = smem + buf * TS::STAGE_BYTES;
     float* sAv = reinterpret_cast<float*>(base + TS::A_VAL);
     uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);
@@ -247,7 +341,8 @@ emu_gemm_kernel(const GemmParams p) {
       const int c = tid + r * NT;
       if (c < A_CHUNKS) {
         const int row = c / (BK / 16), h = c % (BK / 16);
-        const uint32_t w[4] = {ra[r].x, ra[r].y, ra[r].z, ra[r].w};
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + row * BK + h * 16);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const uint2 d = lutA[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
@@ -261,7 +356,8 @@ emu_gemm_kernel(const GemmParams p) {
       const int c = tid + r * NT;
       if (c < B_CHUNKS) {
         const int col = c / (BK / 16), h = c % (BK / 16);
-        const uint32_t w[4] = {rb[r].x, rb[r].y, rb[r].z, rb[r].w};
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + TS::RAW_A + col * BK + h * 16);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const uint2 d = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
@@ -280,13 +376,26 @@ emu_gemm_kernel(const GemmParams p) {
     for (int j = 0; j < TN; ++j) { cp[i][j] = 0.0f; accs[i][j] = 0.0f; }
   int blocks_in_chunk = 0;
 
-  __syncthreads();                       // tables ready
-  if (n_stages > 0) {
-    load_stage(0);
-    store_stage(0);
-    if (n_stages > 1) load_stage(1);
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8u * i, 1u);
+    fence_mbar_init();
   }
-  __syncthreads();
+  __syncthreads();                       // tables and barriers ready
+  if (tid == 0)
+    for (int64_t st = 0; st < NS && st < n_stages; ++st) issue(st);
+  bool timed_out = false;
+  if (n_stages > 0) {
+    timed_out = !mbar_wait_bounded(bar0, 0u, kWaitPolls);
+    decode_stage(0, 0);
+  }
+  if (__syncthreads_or(timed_out)) {
+    if (tid == 0) atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+    return;
+  }
+  if (tid == 0 && NS < n_stages) {
+    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
+    issue(NS);
+  }
 
   for (int64_t st = 0; st < n_stages; ++st) {
     const unsigned char* base = smem + (st & 1) * TS::STAGE_BYTES;
@@ -400,12 +509,21 @@ emu_gemm_kernel(const GemmParams p) {
         }
       }
     }
-    // decode the next stage into the other buffer, prefetch the one after
+    // decode the next stage into the other buffer; refill its ring slot
     if (st + 1 < n_stages) {
-      store_stage((int)((st + 1) & 1));
-      if (st + 2 < n_stages) load_stage(st + 2);
+      const int64_t nx = st + 1;
+      timed_out = !mbar_wait_bounded(bar0 + 8u * (uint32_t)(nx % NS), (uint32_t)((nx / NS) & 1),
+                                     kWaitPolls);
+      decode_stage(nx, (int)(nx & 1));
     }
-    __syncthreads();
+    if (__syncthreads_or(timed_out)) {
+      if (tid == 0) atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+      return;
+    }
+    if (tid == 0 && st + 1 + NS < n_stages) {
+      fence_proxy_async();
+      issue(st + 1 + NS);
+    }
   }
 
   // chain result (fp32 accumulator of this split)
@@ -434,6 +552,7 @@ emu_gemm_kernel(const GemmParams p) {
     return;
   }
   const float alpha = fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b));
+  const OutStore store(p);
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
     const int64_t m = m0 + ty * TM + i;
@@ -442,19 +561,7 @@ emu_gemm_kernel(const GemmParams p) {
     for (int j = 0; j < TN; ++j) {
       const int64_t n = n0 + tx * TN + j;
       if (n >= p.N) continue;
-      const float y = fma_plus0(res[i][j], alpha);
-      const bool isnan_y = (__float_as_uint(y) & 0x7FFFFFFFu) > 0x7F800000u;
-      if (p.out_dtype == 0) {
-        reinterpret_cast<uint32_t*>(p.out)[m * p.N + n] = isnan_y ? 0x7FC00000u : __float_as_uint(y);
-      } else if (p.out_dtype == 1) {
-        const __nv_bfloat16 h = __float2bfloat16_rn(y);
-        reinterpret_cast<uint16_t*>(p.out)[m * p.N + n] =
-            isnan_y ? (uint16_t)0x7FC0u : *reinterpret_cast<const uint16_t*>(&h);
-      } else {
-        const __half h = __float2half_rn(y);
-        reinterpret_cast<uint16_t*>(p.out)[m * p.N + n] =
-            isnan_y ? (uint16_t)0x7E00u : *reinterpret_cast<const uint16_t*>(&h);
-      }
+      store(p, m * p.N + n, fma_plus0(res[i][j], alpha));
     }
   }
 }
@@ -467,6 +574,7 @@ constexpr int kMaxSplit = 64;
 __global__ void emu_combine_kernel(const GemmParams p, int pairwise) {
   const int64_t MN = p.M * p.N;
   const float alpha = fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b));
+  const OutStore store(p);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN;
        i += (int64_t)gridDim.x * blockDim.x) {
     float acc;
@@ -485,17 +593,25 @@ __global__ void emu_combine_kernel(const GemmParams p, int pairwise) {
       }
       acc = v[0];
     }
-    const float y = fma_plus0(acc, alpha);
-    const bool isnan_y = (__float_as_uint(y) & 0x7FFFFFFFu) > 0x7F800000u;
-    if (p.out_dtype == 0) {
-      reinterpret_cast<uint32_t*>(p.out)[i] = isnan_y ? 0x7FC00000u : __float_as_uint(y);
-    } else if (p.out_dtype == 1) {
-      const __nv_bfloat16 h = __float2bfloat16_rn(y);
-      reinterpret_cast<uint16_t*>(p.out)[i] = isnan_y ? (uint16_t)0x7FC0u : *reinterpret_cast<const uint16_t*>(&h);
-    } else {
-      const __half h = __float2half_rn(y);
-      reinterpret_cast<uint16_t*>(p.out)[i] = isnan_y ? (uint16_t)0x7E00u : *reinterpret_cast<const uint16_t*>(&h);
-    }
+    store(p, i, fma_plus0(acc, alpha));
+  }
+}
+
+// Self-test of the bounded wait: an mbarrier expecting two arrivals gets one, so
+// its phase never completes; the wait gives up after `polls` polls and records
+// kStatusWaitTimeout, exactly as the GEMM kernel does when a TMA load never lands.
+__global__ void emu_wait_timeout_selftest_kernel(uint32_t polls) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 2u);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(b);
+  const bool ok = mbar_wait_bounded(b, 0u, polls);
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) atomicExch(&g_emu_device_status, kStatusWaitTimeout);
   }
 }
 
@@ -503,16 +619,10 @@ __global__ void emu_combine_kernel(const GemmParams p, int pairwise) {
 __global__ void emu_fill_k0_kernel(const GemmParams p) {
   const int64_t MN = p.M * p.N;
   const float y = fma_plus0(0.0f, fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b)));
-  const bool isnan_y = (__float_as_uint(y) & 0x7FFFFFFFu) > 0x7F800000u;
+  const OutStore store(p);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < MN;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (p.out_dtype == 0) {
-      reinterpret_cast<uint32_t*>(p.out)[i] = isnan_y ? 0x7FC00000u : __float_as_uint(y);
-    } else {
-      const uint16_t nanv = p.out_dtype == 1 ? 0x7FC0u : 0x7E00u;
-      reinterpret_cast<uint16_t*>(p.out)[i] = isnan_y ? nanv : (uint16_t)0u;
-    }
-  }
+       i += (int64_t)gridDim.x * blockDim.x)
+    store(p, i, y);
 }
 
 }  // namespace emu

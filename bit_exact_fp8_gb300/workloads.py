@@ -17,7 +17,7 @@ Every array is returned as raw FP8 codes (numpy uint8):
 from __future__ import annotations
 
 from dataclasses import dataclass, replace
-from typing import Dict, List
+from typing import Dict, List, Optional
 
 import numpy as np
 import torch
@@ -83,6 +83,7 @@ class Case:
     seed: int = 0
     sigma_a: float = 40.0
     sigma_b: float = 40.0
+    scale_result: Optional[float] = None   # fp8 outputs: multiplier after the scales
 
     @property
     def macs(self) -> int:

@@ -56,8 +56,13 @@ extern "C" {
    (bias 15, exponent 31 = Inf/NaN). */
 typedef enum { EMU_E4M3FN = 0, EMU_E5M2 = 1 } emu_fp8_t;
 
-/* Output dtypes: fp32 (the epilogue's y), bf16 or fp16 rounded to nearest even from y. */
-typedef enum { EMU_OUT_F32 = 0, EMU_OUT_BF16 = 1, EMU_OUT_F16 = 2 } emu_out_t;
+/* Output dtypes: fp32 (the epilogue's y), bf16 or fp16 rounded to nearest even from y,
+   or FP8 (E4M3FN, E5M2): y times scale_result (a separate fp32 multiply, when given)
+   rounded to nearest even and saturated to the format's largest finite value; NaN is
+   0x7F ("Validation evidence", table "Claims and their recordings", fp8-output row). */
+typedef enum {
+  EMU_OUT_F32 = 0, EMU_OUT_BF16 = 1, EMU_OUT_F16 = 2, EMU_OUT_E4M3FN = 3, EMU_OUT_E5M2 = 4
+} emu_out_t;
 
 /* Instruction/platform preset ("Validation evidence", H100 PCIe probe table and
    "Claims and their recordings").  The kernels implement block_width 16 or 32,
@@ -116,6 +121,26 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a,
                   void* stream);
 
 /*
+ * emu_scaled_mm with torch._scaled_mm's scale_result: a device pointer to one fp32
+ * that multiplies y, as a separate fp32 multiply, before the FP8 output conversion
+ * ("Validation evidence", table "Claims and their recordings": "scale_result is a
+ * separate fp32 multiply before saturation to the format's maximum").  NULL means
+ * none; a non-NULL scale_result with a non-FP8 output returns EMU_EUNSUPPORTED, and
+ * e4m3 x e4m3 -> e5m2 returns EMU_EREJECT (cuBLASLt refuses it).  emu_scaled_mm is
+ * this call with scale_result = NULL.
+ */
+int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a,
+                     const uint8_t* B, emu_fp8_t fmt_b,
+                     int64_t M, int64_t N, int64_t K,
+                     const float* scale_a, const float* scale_b,
+                     const float* scale_result,
+                     void* out, emu_out_t out_dtype,
+                     int32_t fast_accum, int32_t split_S,
+                     const emu_preset_t* preset,
+                     void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/*
  * emu_scaled_mm_noalloc: emu_scaled_mm for callers that cannot allocate device
  * memory. (This entry point is an addition of this library; the documentation
  * pages have no counterpart.)
@@ -155,6 +180,23 @@ int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a,
                           int32_t fast_accum, int32_t split_S,
                           const emu_preset_t* preset,
                           void* stream);
+
+/*
+ * Device status of the library on the current device: *status = 0, or 1 when a
+ * kernel's wait for its TMA loads gave up (each wait polls a bounded number of
+ * times instead of hanging; the CTA then returns early and the outputs of that
+ * call are not valid).  Synchronous: it waits for the device.  reset != 0 clears
+ * the status afterwards.  Returns EMU_OK or EMU_EINVAL/EMU_ECUDA.
+ */
+int emu_device_status(int32_t* status, int32_t reset);
+
+/*
+ * Self-test of the bounded wait: enqueues a one-CTA kernel whose barrier can never
+ * complete, so its wait gives up after a short limit and sets the device status
+ * to 1 (read it with emu_device_status).  It exercises the failure path without a
+ * fault or a hang; the pages have no counterpart.
+ */
+int emu_selftest_wait_timeout(void* stream);
 
 /* Message of the last error returned on the calling host thread ("" if none). */
 const char* emu_last_error(void);

@@ -8,13 +8,16 @@ import torch
 import oracle
 
 TORCH_FP8 = {"e4m3fn": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
-TORCH_OUT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+TORCH_OUT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16,
+             "e4m3fn": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 def out_bits(y: torch.Tensor) -> np.ndarray:
     y = y.cpu()
     if y.dtype == torch.float32:
         return y.view(torch.int32).numpy().view(np.uint32)
+    if y.element_size() == 1:
+        return y.view(torch.uint8).numpy().copy()
     return y.view(torch.int16).numpy().view(np.uint16)
 
 
@@ -31,7 +34,9 @@ def gpu_run(cs, a: np.ndarray, b: np.ndarray, *, out=None, splitk=None, preset=N
     if out is None and prefill is not None:
         out = torch.empty((a.shape[0], b.shape[0]), dtype=od, device=dev)
         out.view(torch.uint8).fill_(prefill)
-    y = scaled_mm(A, Bt.t(), sa, sb, out_dtype=od, use_fast_accum=cs.fast_accum,
+    sr = None if cs.scale_result is None else torch.tensor(cs.scale_result, dtype=torch.float32,
+                                                            device=dev)
+    y = scaled_mm(A, Bt.t(), sa, sb, scale_result=sr, out_dtype=od, use_fast_accum=cs.fast_accum,
                   splitk=cs.split_S if splitk is None else splitk,
                   preset=cs.preset if preset is None else preset, out=out)
     torch.cuda.synchronize()
@@ -40,13 +45,14 @@ def gpu_run(cs, a: np.ndarray, b: np.ndarray, *, out=None, splitk=None, preset=N
 
 def oracle_full(cs, a, b, preset=None):
     return oracle.scaled_mm(a, b, cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
-                            cs.fast_accum, cs.split_S, cs.preset if preset is None else preset)
+                            cs.fast_accum, cs.split_S, cs.preset if preset is None else preset,
+                            scale_result=cs.scale_result)
 
 
 def oracle_sampled(cs, a, b, im, jn, preset=None):
     acc = oracle.acc_sampled(a, b, cs.fmt_a, cs.fmt_b, im, jn, cs.fast_accum, cs.split_S,
                              cs.preset if preset is None else preset)
-    return oracle.epilogue(acc, cs.scale_a, cs.scale_b, cs.out_dtype)
+    return oracle.epilogue(acc, cs.scale_a, cs.scale_b, cs.out_dtype, scale_result=cs.scale_result)
 
 
 def sample_indices(M: int, N: int, count: int, seed: int = 0):

@@ -77,7 +77,7 @@ def call(lib, **kw):
     (dict(A=FAKE + 8), -2),                       # misaligned storage
     (dict(out=FAKE + 4), -2),
     (dict(fmt_a=2), -1),
-    (dict(out_dtype=3), -1),
+    (dict(out_dtype=5), -1),
     (dict(M=-1), -1),
     (dict(split_S=0), -1),
     (dict(split_S=65), -3),
@@ -122,7 +122,7 @@ def test_python_api_rejects_cpu_and_unsupported():
     one = torch.ones(())
     with pytest.raises(UnsupportedFeatureError):
         scaled_mm(x, w.t(), one, one, bias=torch.zeros(16))
-    with pytest.raises(UnsupportedFeatureError):
+    with pytest.raises(ValueError):                  # scale_result must live on the GPU
         scaled_mm(x, w.t(), one, one, scale_result=one)
     with pytest.raises(ReferenceRejectsError):
         scaled_mm(x.float(), w.t(), one, one)
@@ -130,3 +130,15 @@ def test_python_api_rejects_cpu_and_unsupported():
         scaled_mm(x, w.t(), one, one)
     assert issubclass(ReferenceRejectsError, RuntimeError)
     assert issubclass(UnsupportedFeatureError, NotImplementedError)
+
+
+def test_fp8_output_argument_checks(lib):
+    L = lib.load()
+    p = lib.emu_preset_get("hopper")
+    def ex(fa, fb, od, sr):
+        return lib.emu_scaled_mm_ex(FAKE, fa, FAKE, fb, 16, 64, 256, FAKE, FAKE, sr, FAKE, od,
+                                    1, 1, p, 0, 0, 0)
+    assert ex(0, 0, 4, 0) == -2          # cuBLASLt refuses e4m3 x e4m3 -> e5m2
+    assert ex(0, 0, 1, FAKE) == -3       # scale_result with a non-fp8 output
+    assert ex(0, 0, 5, 0) == -1          # unknown output dtype
+    assert L is not None

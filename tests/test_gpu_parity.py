@@ -199,5 +199,32 @@ def test_rejections():
         scaled_mm(x4, x4.t(), torch.ones(16, 1, device=dev), one, out_dtype=bf)  # row-wise
     with pytest.raises(UnsupportedFeatureError):
         scaled_mm(x4, x4.t(), one, one, out_dtype=bf, splitk=65)
-    with pytest.raises(UnsupportedFeatureError):
-        scaled_mm(x4, x4.t(), one, one)                    # fp8 output (torch default dtype)
+
+
+# fp8 outputs: scale_result as a separate fp32 multiply, then saturating
+# round-to-nearest-even conversion ("Validation evidence", claims table)
+@pytest.mark.parametrize("od", ("e4m3fn", "e5m2"))
+@pytest.mark.parametrize("sr", (None, 0.37, -3.0, 1e-6))
+@pytest.mark.parametrize("fa,fb", (("e4m3fn", "e4m3fn"), ("e4m3fn", "e5m2"), ("e5m2", "e4m3fn")))
+def test_fp8_outputs(od, sr, fa, fb):
+    if fa == fb == "e4m3fn" and od == "e5m2":
+        pytest.skip("rejected: e4m3 x e4m3 -> e5m2")
+    for fast, S in ((True, 1), (False, 3)):
+        cs = W.Case(f"fp8-{od}-{sr}-{fa}-{fb}-{S}", 70, 96, 528, fa, fb, od, fast_accum=fast,
+                    split_S=S, gen="mixed", seed=11, scale_a=1.0, scale_b=0.25, scale_result=sr)
+        full_check(cs)
+
+
+def test_fp8_output_rejection_and_k0():
+    from bit_exact_fp8_gb300 import ReferenceRejectsError, scaled_mm
+    dev = torch.device("cuda:0")
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    x = torch.zeros(16, 32, device=dev).to(torch.float8_e4m3fn)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm(x, x.t(), one, one, out_dtype=torch.float8_e5m2)
+    x0 = torch.zeros(5, 0, device=dev).to(torch.float8_e4m3fn)
+    w0 = torch.zeros(16, 0, device=dev).to(torch.float8_e4m3fn)
+    y = scaled_mm(x0, w0.t(), one, one, scale_result=-one, out_dtype=torch.float8_e4m3fn)
+    torch.cuda.synchronize()
+    # fma(+0, alpha, +0) = +0, times -1 = -0: code 0x80
+    assert (y.view(torch.uint8) == 0x80).all()

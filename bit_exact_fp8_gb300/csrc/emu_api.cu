@@ -41,22 +41,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 //   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32 (skinny, split-K)
 //   K8   1 x 2,  4 x  4 x 8 lanes, BK 64:  4 x  8, each block split over 8 lanes
 //   K4   1 x 2,  4 x  8 x 4 lanes, BK 64:  4 x 16, each block split over 4 lanes
+//   K8H, K4H: the same with BK 128, so a stage's barrier and wait are shared by four
+//        32-product blocks: about 25% faster when an SM holds one or two CTAs (latency
+//        bound), about 15% slower when it holds four or more, so the chooser only swaps
+//        them in for K8/K4 in the first case, and only where every split starts on a
+//        multiple of 128 (k-tiles of 128, or no split)
 //        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
 //        CTA tile must stay tiny for every SM to get work)
 struct TileInfo {
   const char* name;
   int tm, tn, bm, bn, threads, resident, bk, g;  // resident: CTAs per SM for the cost model
   double cost;                                   // relative instructions per MAC
+  int deep;                                      // BK-128 variant for light SM loads, or -1
 };
 constexpr TileInfo kTiles[] = {
-    {"L", 8, 4, 128, 64, 256, 2, 32, 1, 1.00},
-    {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15},
-    {"M32", 4, 4, 64, 32, 128, 3, 32, 1, 1.05},
-    {"S", 2, 2, 16, 32, 128, 4, 32, 1, 1.50},
-    {"K8", 1, 2, 4, 8, 128, 8, 64, 8, 3.00},
-    {"K4", 1, 2, 4, 16, 128, 8, 64, 4, 2.40},
+    {"L", 8, 4, 128, 64, 256, 2, 32, 1, 1.00, -1},
+    {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15, -1},
+    {"M32", 4, 4, 64, 32, 128, 3, 32, 1, 1.05, -1},
+    {"S", 2, 2, 16, 32, 128, 4, 32, 1, 1.50, -1},
+    {"K8", 1, 2, 4, 8, 128, 8, 64, 8, 3.00, 6},
+    {"K4", 1, 2, 4, 16, 128, 8, 64, 4, 2.40, 7},
+    {"K8H", 1, 2, 4, 8, 128, 7, 128, 8, 3.00, -1},
+    {"K4H", 1, 2, 4, 16, 128, 4, 128, 4, 2.40, -1},
 };
-constexpr int kNumTiles = 6;
+constexpr int kNumTiles = 8;
+constexpr int kFirstDeep = 6;   // K8H, K4H: reached only through a base tile's `deep`
 constexpr int kSMs = 152;
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
@@ -140,22 +149,27 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
   }
   auto usable = [&](int t) { return p.S == 1 || p.ktile % kTiles[t].bk == 0; };
   if (forced >= 0 && usable(forced)) return forced;
+  auto ctas_of = [&](const TileInfo& ti) {
+    return (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
+  };
   int best = -1;
   double best_cost = 0.0;
-  for (int t = 0; t < kNumTiles; ++t) {
+  for (int t = 0; t < kFirstDeep; ++t) {
     if (!usable(t)) continue;
     TileInfo ti = kTiles[t];
     if (slow && t == 0) {                  // the large tile's slow variant needs 173 registers
       ti.resident = 1;
       ti.cost *= 1.1;
     }
-    const double ctas = (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
+    const double ctas = ctas_of(ti);
     const double per_sm = std::ceil(ctas / kSMs);
     const double t_issue = per_sm * ti.bm * ti.bn * ti.cost / 128.0;
     const double t_latency = std::ceil(per_sm / ti.resident) * ti.tm * ti.tn * ti.cost * 2.0 / ti.g;
     const double est = std::max(t_issue, t_latency);
     if (best < 0 || est < best_cost) { best = t; best_cost = est; }
   }
+  const int deep = kTiles[best].deep;
+  if (deep >= 0 && usable(deep) && ctas_of(kTiles[deep]) <= 2.0 * kSMs) return deep;
   return best;
 }
 
@@ -166,7 +180,9 @@ int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
     case 2: return launch_tile<4, 4, 16, 8, 32, false>(p, blk, slow, st);
     case 3: return launch_tile<2, 2, 8, 16, 32, true>(p, blk, slow, st);
     case 4: return launch_tile<1, 2, 4, 4, 64, false, 8>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 64, false, 4>(p, blk, slow, st);
+    case 5: return launch_tile<1, 2, 4, 8, 64, false, 4>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 128, false, 4>(p, blk, slow, st);
   }
 }
 

@@ -54,6 +54,8 @@ struct TileInfo {
   double cost;                                   // relative instructions per MAC
   int deep;                                      // BK-128 variant for light SM loads, or -1
 };
+// resident is also the kernel's __launch_bounds__ minimum (the large tile's slow
+// variant: 1), which holds ptxas to 65536 / (resident * threads) registers
 constexpr TileInfo kTiles[] = {
     {"L", 8, 4, 128, 64, 256, 2, 32, 1, 1.00, -1},
     {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15, -1},
@@ -100,10 +102,10 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_
   return EMU_OK;
 }
 
-template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G>
+template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G, int MINB>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G, MINB>;
   // the dynamic shared memory limit is a per-function, per-device attribute
   static bool configured[64] = {false};
   int dev = 0;
@@ -123,14 +125,16 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   return EMU_OK;
 }
 
-template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G = 1>
+// MINB, MINB_SLOW: the CTAs per SM the fast and slow variants are meant to keep
+// resident (the register budget ptxas is held to)
+template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G, int MINB, int MINB_SLOW = MINB>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G>(p, st)
-                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G, MINB_SLOW>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G, MINB>(p, st);
   }
-  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G>(p, st)
-              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G>(p, st);
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G, MINB_SLOW>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G, MINB>(p, st);
 }
 
 // Pick the tile with the lowest estimated time per K element, in SM cycles: the
@@ -175,14 +179,14 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   switch (choose_tile(p, slow)) {
-    case 0: return launch_tile<8, 4, 16, 16, 32, false>(p, blk, slow, st);
-    case 1: return launch_tile<4, 2, 16, 20, 64, true>(p, blk, slow, st);
-    case 2: return launch_tile<4, 4, 16, 8, 32, false>(p, blk, slow, st);
-    case 3: return launch_tile<2, 2, 8, 16, 32, true>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 4, 64, false, 8>(p, blk, slow, st);
-    case 5: return launch_tile<1, 2, 4, 8, 64, false, 4>(p, blk, slow, st);
-    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 128, false, 4>(p, blk, slow, st);
+    case 0: return launch_tile<8, 4, 16, 16, 32, false, 1, 2, 1>(p, blk, slow, st);
+    case 1: return launch_tile<4, 2, 16, 20, 64, true, 1, 1>(p, blk, slow, st);
+    case 2: return launch_tile<4, 4, 16, 8, 32, false, 1, 3>(p, blk, slow, st);
+    case 3: return launch_tile<2, 2, 8, 16, 32, true, 1, 4>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 4, 64, false, 8, 8>(p, blk, slow, st);
+    case 5: return launch_tile<1, 2, 4, 8, 64, false, 4, 8>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8, 7>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 128, false, 4, 4>(p, blk, slow, st);
   }
 }
 

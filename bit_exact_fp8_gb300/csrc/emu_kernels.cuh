@@ -247,12 +247,12 @@ struct TileShape {
   static constexpr int LUT_BYTES = 2 * 256 * 8;
   static constexpr int LUT_OFF = RAW_OFF + NS * RAW_STAGE;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8;
+  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8;   // one "slot full" mbarrier per slot
   static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
 };
 
-template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G>
-__global__ void __launch_bounds__(WM * WN * G)
+template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G, int MINB>
+__global__ void __launch_bounds__(WM * WN * G, MINB)
 emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB) {
   using TS = TileShape<TM, TN, WM, WN, BK_, G>;
@@ -265,8 +265,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   constexpr int NBLK = BK / BLK;
   constexpr int A_CHUNKS = BM * BK / 16;
   constexpr int B_CHUNKS = BN * BK / 16;
-  constexpr int A_PER = (A_CHUNKS + NT - 1) / NT;
-  constexpr int B_PER = (B_CHUNKS + NT - 1) / NT;
+  constexpr int AB_PER = (A_CHUNKS + B_CHUNKS + NT - 1) / NT;
   constexpr int NS = TS::NS;
   static_assert(TN % 2 == 0, "labels are paired along N");
 
@@ -319,7 +318,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   };
   // one thread: start the TMA loads of stage st into its ring slot.  Boxes reaching
   // past M, N or K are zero-filled, and zero codes are neutral in every block.
+  int64_t issued = 0;                        // stages whose loads thread 0 started
   auto issue = [&](int64_t st) {
+    issued = st + 1;
     const int slot = (int)(st % NS);
     const uint32_t bar = bar0 + 8u * slot;
     const uint32_t dst = smem_u32(smem + TS::RAW_OFF + slot * TS::RAW_STAGE);
@@ -336,8 +337,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);
     float* sBv = reinterpret_cast<float*>(base + TS::B_VAL);
     int16_t* sBl = reinterpret_cast<int16_t*>(base + TS::B_LAB);
+    // A chunks first, then B chunks, dealt round-robin over all threads, so that
+    // no thread decodes more than ceil((A + B) / NT) chunks
 #pragma unroll
-    for (int r = 0; r < A_PER; ++r) {
+    for (int r = 0; r < AB_PER; ++r) {
       const int c = tid + r * NT;
       if (c < A_CHUNKS) {
         const int row = c / (BK / 16), h = c % (BK / 16);
@@ -349,13 +352,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           sAv[(h * 16 + j) * BM + row] = __uint_as_float(d.x);
           sAl[(h * 16 + j) * BM + row] = d.y;
         }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < B_PER; ++r) {
-      const int c = tid + r * NT;
-      if (c < B_CHUNKS) {
-        const int col = c / (BK / 16), h = c % (BK / 16);
+      } else if (c < A_CHUNKS + B_CHUNKS) {
+        const int cb = c - A_CHUNKS;
+        const int col = cb / (BK / 16), h = cb % (BK / 16);
         const uint4 q = *reinterpret_cast<const uint4*>(raw + TS::RAW_A + col * BK + h * 16);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -383,28 +382,27 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   __syncthreads();                       // tables and barriers ready
   if (tid == 0)
     for (int64_t st = 0; st < NS && st < n_stages; ++st) issue(st);
-  bool timed_out = false;
-  if (n_stages > 0) {
-    timed_out = !mbar_wait_bounded(bar0, 0u, kWaitPolls);
-    decode_stage(0, 0);
-  }
-  if (__syncthreads_or(timed_out)) {
-    if (tid == 0) atomicExch(&g_emu_device_status, kStatusWaitTimeout);
-    return;
-  }
-  if (tid == 0 && NS < n_stages) {
-    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
-    issue(NS);
-  }
+  auto full_wait = [&](int64_t st) {
+    return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st % NS), (uint32_t)((st / NS) & 1), kWaitPolls);
+  };
+  // after a wait gave up: record it; thread 0 waits (bounded) for its loads still in
+  // flight from stage `from` on, so that none lands after the CTA has exited
+  auto give_up = [&](int64_t from) {
+    atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+    if (tid == 0)
+      for (int64_t x = from; x < issued; ++x) (void)full_wait(x);
+  };
 
-  for (int64_t st = 0; st < n_stages; ++st) {
-    const unsigned char* base = smem + (st & 1) * TS::STAGE_BYTES;
+  // one K-stage of every block chain, from the decoded buffer at `base`
+  auto compute_stage = [&](const unsigned char* base) {
     const float* sAv = reinterpret_cast<const float*>(base + TS::A_VAL);
     const uint32_t* sAl = reinterpret_cast<const uint32_t*>(base + TS::A_LAB);
     const float* sBv = reinterpret_cast<const float*>(base + TS::B_VAL);
     const uint32_t* sBl2 = reinterpret_cast<const uint32_t*>(base + TS::B_LAB);
 
-#pragma unroll
+    // slow chains: the blocks of a stage stay a loop (a restart may fall after any
+    // of them; unrolled, the 64 x 40 tile's 32-product variant spilled registers)
+#pragma unroll (SLOW ? 1 : NBLK)
     for (int bb = 0; bb < NBLK; ++bb) {
       const int k0 = bb * BLK;
       // ---- pass 1: block maximum of the product label sums (independent of the
@@ -509,17 +507,27 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         }
       }
     }
-    // decode the next stage into the other buffer; refill its ring slot
+  };
+
+  // decode stage st + 1 into the other buffer while nobody reads it, then one
+  // barrier per stage; thread 0 refills the ring slot everyone has decoded
+  bool timed_out = false;
+  if (n_stages > 0) {
+    timed_out = !full_wait(0);
+    decode_stage(0, 0);
+  }
+  if (__syncthreads_or(timed_out)) { give_up(0); return; }
+  if (tid == 0 && NS < n_stages) {
+    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
+    issue(NS);
+  }
+  for (int64_t st = 0; st < n_stages; ++st) {
+    compute_stage(smem + (st & 1) * TS::STAGE_BYTES);
     if (st + 1 < n_stages) {
-      const int64_t nx = st + 1;
-      timed_out = !mbar_wait_bounded(bar0 + 8u * (uint32_t)(nx % NS), (uint32_t)((nx / NS) & 1),
-                                     kWaitPolls);
-      decode_stage(nx, (int)(nx & 1));
+      timed_out = !full_wait(st + 1);
+      decode_stage(st + 1, (int)((st + 1) & 1));
     }
-    if (__syncthreads_or(timed_out)) {
-      if (tid == 0) atomicExch(&g_emu_device_status, kStatusWaitTimeout);
-      return;
-    }
+    if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
     if (tid == 0 && st + 1 + NS < n_stages) {
       fence_proxy_async();
       issue(st + 1 + NS);

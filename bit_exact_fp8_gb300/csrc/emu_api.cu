@@ -85,18 +85,27 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D u8 tensor map of a K-contiguous operand [rows, K] with box [box_rows, box_k]
+// 2-D u8 tensor map of a K-contiguous operand [rows, K] with box [box_rows, box_k];
+// swizzled: the 16-byte chunks of each box row are permuted by the TMA swizzle of
+// width box_k bytes (32, 64 or 128)
 int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_t K,
-                     int box_rows, int box_k) {
+                     int box_rows, int box_k, bool swizzled) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(EMU_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K};
   const cuuint32_t box[2] = {(cuuint32_t)box_k, (cuuint32_t)box_rows};
   const cuuint32_t elem[2] = {1u, 1u};
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzled) {
+    if (box_k == 32) swz = CU_TENSOR_MAP_SWIZZLE_32B;
+    else if (box_k == 64) swz = CU_TENSOR_MAP_SWIZZLE_64B;
+    else if (box_k == 128) swz = CU_TENSOR_MAP_SWIZZLE_128B;
+    else return fail(EMU_EUNSUPPORTED, "no swizzle for %d-byte box rows", box_k);
+  }
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(base), dims,
                          strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(EMU_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return EMU_OK;
@@ -115,9 +124,9 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
   CUtensorMap tmA, tmB;
-  int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK);
+  int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK, TS::SWZ);
   if (rc != EMU_OK) return rc;
-  rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK);
+  rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK, TS::SWZ);
   if (rc != EMU_OK) return rc;
   dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)((p.M + TS::BM - 1) / TS::BM),
             (unsigned)p.S);

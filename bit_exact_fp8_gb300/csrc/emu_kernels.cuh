@@ -231,24 +231,32 @@ struct TileShape {
   static constexpr int BM = WM * TM;
   static constexpr int BN = WN * TN;
   static constexpr int BK = BK_;
-  // one stage buffer: A values [BK][BM] f32, A labels [BK][BM] u32 (label in both
-  // halves), B values [BK][BN] f32, B labels [BK][BN] i16
+  // SWZ: the raw boxes arrive swizzled (TMA 32/64/128-byte swizzle, matching BK) and a
+  // warp decodes 32 consecutive rows of one 16-code chunk, so that its shared stores
+  // hit 32 distinct banks and its 16-byte raw reads 8 distinct bank quads
+  static constexpr bool SWZ = BM >= 32 && BN >= 32 && (BK == 32 || BK == 64 || BK == 128);
+  // ring of raw FP8 boxes filled by TMA, first in shared memory: A [BM][BK] then
+  // B [BN][BK] bytes per slot; with SWZ every box starts on a 1024-byte boundary
+  // (the swizzle pattern's period), the ring's base included
+  static constexpr int RAW_A = BM * BK;
+  static constexpr int RAW_B = BN * BK;
+  static constexpr int RAW_ALIGN = SWZ ? 1024 : 128;
+  static constexpr int RAW_STAGE = ((RAW_A + RAW_B) + RAW_ALIGN - 1) / RAW_ALIGN * RAW_ALIGN;
+  static constexpr int NS = RAW_STAGE <= 1024 ? 8 : (BM >= 128 ? 3 : 4);   // ring depth
+  // one decoded stage buffer: A values [BK][BM] f32, A labels [BK][BM] u32 (label in
+  // both halves), B values [BK][BN] f32, B labels [BK][BN] i16
   static constexpr int A_VAL = 0;
   static constexpr int A_LAB = A_VAL + BK * BM * 4;
   static constexpr int B_VAL = A_LAB + BK * BM * 4;
   static constexpr int B_LAB = B_VAL + BK * BN * 4;
   static constexpr int STAGE_BYTES = ((B_LAB + BK * BN * 2) + 127) / 128 * 128;
-  // ring of raw FP8 boxes filled by TMA: A [BM][BK] then B [BN][BK] bytes per slot
-  static constexpr int RAW_A = BM * BK;
-  static constexpr int RAW_B = BN * BK;
-  static constexpr int RAW_STAGE = ((RAW_A + RAW_B) + 127) / 128 * 128;
-  static constexpr int NS = RAW_STAGE <= 1024 ? 8 : (BM >= 128 ? 3 : 4);   // ring depth
-  static constexpr int RAW_OFF = 2 * STAGE_BYTES;
+  static constexpr int STAGE_OFF = NS * RAW_STAGE;
   static constexpr int LUT_BYTES = 2 * 256 * 8;
-  static constexpr int LUT_OFF = RAW_OFF + NS * RAW_STAGE;
+  static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8;   // one "slot full" mbarrier per slot
-  static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
+  // dynamic shared memory to request: the layout plus room to align its base
+  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8 + RAW_ALIGN;
+  static_assert(RAW_A % RAW_ALIGN == 0, "the B box of a slot starts aligned");
 };
 
 template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G, int MINB>
@@ -269,7 +277,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   constexpr int NS = TS::NS;
   static_assert(TN % 2 == 0, "labels are paired along N");
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  // layout base: the dynamic buffer rounded up to the raw ring's alignment
+  unsigned char* const smem =
+      smem_dyn + ((TS::RAW_ALIGN - (smem_u32(smem_dyn) & (TS::RAW_ALIGN - 1))) & (TS::RAW_ALIGN - 1));
   uint2* lutA = reinterpret_cast<uint2*>(smem + TS::LUT_OFF);
   uint2* lutB = lutA + 256;
   const uint32_t bar0 = smem_u32(smem + TS::BAR_OFF);
@@ -323,7 +334,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     issued = st + 1;
     const int slot = (int)(st % NS);
     const uint32_t bar = bar0 + 8u * slot;
-    const uint32_t dst = smem_u32(smem + TS::RAW_OFF + slot * TS::RAW_STAGE);
+    const uint32_t dst = smem_u32(smem + slot * TS::RAW_STAGE);
     const int k = stage_k(st);
     mbar_arrive_expect_tx(bar, (uint32_t)(TS::RAW_A + TS::RAW_B));
     tma_load_2d(dst, &tmA, k, (int)m0, bar);
@@ -331,20 +342,28 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   };
   // all threads: decode the raw slot of stage st into operand buffer buf
   auto decode_stage = [&](int64_t st, int buf) {
-    const unsigned char* raw = smem + TS::RAW_OFF + (int)(st % NS) * TS::RAW_STAGE;
-    unsigned char* base = smem + buf * TS::STAGE_BYTES;
+    const unsigned char* raw = smem + (int)(st % NS) * TS::RAW_STAGE;
+    unsigned char* base = smem + TS::STAGE_OFF + buf * TS::STAGE_BYTES;
     float* sAv = reinterpret_cast<float*>(base + TS::A_VAL);
     uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);
     float* sBv = reinterpret_cast<float*>(base + TS::B_VAL);
     int16_t* sBl = reinterpret_cast<int16_t*>(base + TS::B_LAB);
     // A chunks first, then B chunks, dealt round-robin over all threads, so that
-    // no thread decodes more than ceil((A + B) / NT) chunks
+    // no thread decodes more than ceil((A + B) / NT) chunks.  Chunk h of a box row
+    // sits at 16-byte position h, or with SWZ at h XOR bits 7.. of the row's address.
+    constexpr int HM = BK / 16 - 1;
+    const uint32_t raw_u32 = smem_u32(raw);
+    auto chunk = [&](int off_row, int h) -> uint4 {
+      const int hs = TS::SWZ ? (h ^ (int)(((raw_u32 + (uint32_t)off_row) >> 7) & (uint32_t)HM)) : h;
+      return *reinterpret_cast<const uint4*>(raw + off_row + hs * 16);
+    };
 #pragma unroll
     for (int r = 0; r < AB_PER; ++r) {
       const int c = tid + r * NT;
       if (c < A_CHUNKS) {
-        const int row = c / (BK / 16), h = c % (BK / 16);
-        const uint4 q = *reinterpret_cast<const uint4*>(raw + row * BK + h * 16);
+        const int row = TS::SWZ ? c % BM : c / (BK / 16);
+        const int h = TS::SWZ ? c / BM : c % (BK / 16);
+        const uint4 q = chunk(row * BK, h);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -354,8 +373,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         }
       } else if (c < A_CHUNKS + B_CHUNKS) {
         const int cb = c - A_CHUNKS;
-        const int col = cb / (BK / 16), h = cb % (BK / 16);
-        const uint4 q = *reinterpret_cast<const uint4*>(raw + TS::RAW_A + col * BK + h * 16);
+        const int col = TS::SWZ ? cb % BN : cb / (BK / 16);
+        const int h = TS::SWZ ? cb / BN : cb % (BK / 16);
+        const uint4 q = chunk(TS::RAW_A + col * BK, h);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -522,7 +542,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     issue(NS);
   }
   for (int64_t st = 0; st < n_stages; ++st) {
-    compute_stage(smem + (st & 1) * TS::STAGE_BYTES);
+    compute_stage(smem + TS::STAGE_OFF + (st & 1) * TS::STAGE_BYTES);
     if (st + 1 < n_stages) {
       timed_out = !full_wait(st + 1);
       decode_stage(st + 1, (int)((st + 1) & 1));

@@ -34,41 +34,63 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tile shapes (thread tile TM x TN, CTA WM x WN threads, K-stage BK):
-//   L    8 x 4, 16 x 16 threads, BK 32: 128 x 64 outputs per CTA (large M x N)
-//   M40  4 x 2, 16 x 20 threads, BK 64:  64 x 40 (M <= 64 with wide N: one CTA per SM)
-//   M32  4 x 4, 16 x  8 threads, BK 32:  64 x 32
-//   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32 (skinny, split-K)
+// Tile shapes (thread tile TM x TN, CTA WM x WN threads, K-stage BK); "packed": the
+// pass-2 products, truncations and sums run as f32x2 pairs of adjacent k:
+//   M40  4 x 2, 16 x 20 threads, BK 64:  64 x 40 outputs per CTA, packed (M <= 64 with
+//        wide N: one CTA per SM)
+//   M32  4 x 4, 16 x  8 threads, BK 32:  64 x 32, packed, three CTAs per SM
+//   M64  4 x 4, 16 x 16 threads, BK 32:  64 x 64, packed, two CTAs per SM (slow: one)
+//   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32, packed (skinny, split-K)
 //   K8   1 x 2,  4 x  4 x 8 lanes, BK 64:  4 x  8, each block split over 8 lanes
 //   K4   1 x 2,  4 x  8 x 4 lanes, BK 64:  4 x 16, each block split over 4 lanes
 //   K8H, K4H: the same with BK 128, so a stage's barrier and wait are shared by four
-//        32-product blocks: about 25% faster when an SM holds one or two CTAs (latency
-//        bound), about 15% slower when it holds four or more, so the chooser only swaps
-//        them in for K8/K4 in the first case, and only where every split starts on a
-//        multiple of 128 (k-tiles of 128, or no split)
+//        32-product blocks: faster when an SM holds one or two CTAs (latency bound),
+//        slower when it holds more, so the chooser only swaps them in for K8/K4 in the
+//        first case, and only where every split starts on a multiple of 128
 //        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
-//        CTA tile must stay tiny for every SM to get work)
+//        CTA tile must stay tiny for every SM to get work; one or two products per
+//        lane and block, so they keep scalar FP32)
 struct TileInfo {
   const char* name;
-  int tm, tn, bm, bn, threads, resident, bk, g;  // resident: CTAs per SM for the cost model
-  double cost;                                   // relative instructions per MAC
-  int deep;                                      // BK-128 variant for light SM loads, or -1
+  int tm, tn, bm, bn, threads;
+  int resident, resident_slow;  // CTAs per SM (shared memory and the register budget)
+  int bk, g;
+  // cost model, both measured on the GB300 workloads (SM clocks per K element):
+  double ipm;                   // effective thread instructions per MAC at full load
+  double lat;                   // one CTA alone on an SM
+  double slow_factor;           // slow accumulation's extra cost
+  int deep;                     // BK-128 variant for light SM loads, or -1
 };
-// resident is also the kernel's __launch_bounds__ minimum (the large tile's slow
-// variant: 1), which holds ptxas to 65536 / (resident * threads) registers
+// resident is also the kernel's __launch_bounds__ minimum, which holds ptxas to
+// 65536 / (resident * threads) registers
 constexpr TileInfo kTiles[] = {
-    {"L", 8, 4, 128, 64, 256, 2, 32, 1, 1.00, -1},
-    {"M40", 4, 2, 64, 40, 320, 1, 64, 1, 1.15, -1},
-    {"M32", 4, 4, 64, 32, 128, 3, 32, 1, 1.05, -1},
-    {"S", 2, 2, 16, 32, 128, 4, 32, 1, 1.50, -1},
-    {"K8", 1, 2, 4, 8, 128, 8, 64, 8, 3.00, 6},
-    {"K4", 1, 2, 4, 16, 128, 8, 64, 4, 2.40, 7},
-    {"K8H", 1, 2, 4, 8, 128, 7, 128, 8, 3.00, -1},
-    {"K4H", 1, 2, 4, 16, 128, 4, 128, 4, 2.40, -1},
+    {"M40", 4, 2, 64, 40, 320, 1, 1, 64, 1, 7.2, 150.0, 1.0, -1},
+    {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 5.3, 200.0, 1.0, -1},
+    {"S", 2, 2, 16, 32, 128, 4, 4, 32, 1, 8.0, 63.0, 1.0, -1},
+    {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 51.0, 35.0, 1.0, 6},
+    {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 38.0, 38.4, 1.0, 7},
+    {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, -1},
+    {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 51.0, 25.0, 1.0, -1},
+    {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 38.0, 29.0, 1.0, -1},
 };
 constexpr int kNumTiles = 8;
-constexpr int kFirstDeep = 6;   // K8H, K4H: reached only through a base tile's `deep`
-constexpr int kSMs = 152;
+constexpr bool is_deep_variant(int t) {
+  for (int u = 0; u < kNumTiles; ++u)
+    if (kTiles[u].deep == t) return true;
+  return false;
+}
+// SMs of the current device (152 on a GB300), cached per device
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cached[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                   n > 0) ? n : 152;
+  }
+  return cached[dev];
+}
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -111,10 +133,11 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_
   return EMU_OK;
 }
 
-template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G, int MINB>
+template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G, int MINB,
+          bool PK>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G, MINB>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G, MINB, PK>;
   // the dynamic shared memory limit is a per-function, per-device attribute
   static bool configured[64] = {false};
   int dev = 0;
@@ -136,21 +159,20 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
 
 // MINB, MINB_SLOW: the CTAs per SM the fast and slow variants are meant to keep
 // resident (the register budget ptxas is held to)
-template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G, int MINB, int MINB_SLOW = MINB>
+template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G, int MINB, int MINB_SLOW = MINB,
+          bool PK = true>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G, MINB_SLOW>(p, st)
-                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G, MINB>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G, MINB_SLOW, PK>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G, MINB, PK>(p, st);
   }
-  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G, MINB_SLOW>(p, st)
-              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G, MINB>(p, st);
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G, MINB_SLOW, PK>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G, MINB, PK>(p, st);
 }
 
-// Pick the tile with the lowest estimated time per K element, in SM cycles: the
-// larger of the issue time of the CTAs an SM receives (128 lanes per clock) and
-// the latency-bound time of one thread's instruction stream (about one
-// instruction per two clocks when few warps share a scheduler).
-// EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
+// Pick the tile with the lowest estimated time per K element, in SM clocks: the
+// larger of the issue time of the CTAs an SM receives and the latency-bound time of
+// its waves of resident CTAs.  EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
 int choose_tile(const emu::GemmParams& p, bool slow) {
   static int forced = -2;
   if (forced == -2) {
@@ -165,37 +187,34 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
   auto ctas_of = [&](const TileInfo& ti) {
     return (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
   };
+  const double sms = sm_count();
   int best = -1;
   double best_cost = 0.0;
-  for (int t = 0; t < kFirstDeep; ++t) {
-    if (!usable(t)) continue;
-    TileInfo ti = kTiles[t];
-    if (slow && t == 0) {                  // the large tile's slow variant needs 173 registers
-      ti.resident = 1;
-      ti.cost *= 1.1;
-    }
-    const double ctas = ctas_of(ti);
-    const double per_sm = std::ceil(ctas / kSMs);
-    const double t_issue = per_sm * ti.bm * ti.bn * ti.cost / 128.0;
-    const double t_latency = std::ceil(per_sm / ti.resident) * ti.tm * ti.tn * ti.cost * 2.0 / ti.g;
-    const double est = std::max(t_issue, t_latency);
+  for (int t = 0; t < kNumTiles; ++t) {
+    if (is_deep_variant(t) || !usable(t)) continue;
+    const TileInfo& ti = kTiles[t];
+    const int resident = slow ? ti.resident_slow : ti.resident;
+    const double per_sm = std::ceil(ctas_of(ti) / sms);
+    const double t_issue = per_sm * ti.bm * ti.bn * ti.ipm / 128.0;
+    const double t_latency = std::ceil(per_sm / resident) * ti.lat;
+    const double est = std::max(t_issue, t_latency) * (slow ? ti.slow_factor : 1.0);
     if (best < 0 || est < best_cost) { best = t; best_cost = est; }
   }
   const int deep = kTiles[best].deep;
-  if (deep >= 0 && usable(deep) && ctas_of(kTiles[deep]) <= 2.0 * kSMs) return deep;
+  if (deep >= 0 && usable(deep) && ctas_of(kTiles[deep]) <= 2.0 * sms) return deep;
   return best;
 }
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   switch (choose_tile(p, slow)) {
-    case 0: return launch_tile<8, 4, 16, 16, 32, false, 1, 2, 1>(p, blk, slow, st);
-    case 1: return launch_tile<4, 2, 16, 20, 64, true, 1, 1>(p, blk, slow, st);
-    case 2: return launch_tile<4, 4, 16, 8, 32, false, 1, 3>(p, blk, slow, st);
-    case 3: return launch_tile<2, 2, 8, 16, 32, true, 1, 4>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 4, 64, false, 8, 8>(p, blk, slow, st);
-    case 5: return launch_tile<1, 2, 4, 8, 64, false, 4, 8>(p, blk, slow, st);
-    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8, 7>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 128, false, 4, 4>(p, blk, slow, st);
+    case 0: return launch_tile<4, 2, 16, 20, 64, true, 1, 1>(p, blk, slow, st);
+    case 1: return launch_tile<4, 4, 16, 8, 32, false, 1, 3>(p, blk, slow, st);
+    case 2: return launch_tile<2, 2, 8, 16, 32, true, 1, 4>(p, blk, slow, st);
+    case 3: return launch_tile<1, 2, 4, 4, 64, false, 8, 8, 8, false>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 8, 64, false, 4, 8, 8, false>(p, blk, slow, st);
+    case 5: return launch_tile<4, 4, 16, 16, 32, false, 1, 2, 1>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8, 7, 7, false>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 128, false, 4, 4, 4, false>(p, blk, slow, st);
   }
 }
 

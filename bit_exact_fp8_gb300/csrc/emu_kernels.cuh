@@ -331,6 +331,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   constexpr int A_CHUNKS = BM * BK / 16;
   constexpr int B_CHUNKS = BN * BK / 16;
   constexpr int AB_PER = (A_CHUNKS + B_CHUNKS + NT - 1) / NT;
+  // packed B values: column n = tx * TN + j sits at pair slot (j / 2) * 2WN + 2tx + j % 2
+  // of its k-pair row, so a thread's 16-byte loads of pairs (j, j + 1) are contiguous
+  // across the warp's threads (the identity for TN = 2)
+  auto b_slot = [](int n) { return ((n % TN) / 2) * (2 * WN) + (n / TN) * 2 + (n % 2); };
   constexpr int NS = TS::NS;
   static_assert(TN % 2 == 0, "labels are paired along N");
 
@@ -445,7 +449,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           const uint2 d0 = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
           const uint2 d1 = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3))];
           if (PK) {
-            *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + col) * 2) = make_uint2(d0.x, d1.x);
+            *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
+                make_uint2(d0.x, d1.x);
           } else {
             sBv[(h * 16 + j) * BN + col] = __uint_as_float(d0.x);
             sBv[(h * 16 + j + 1) * BN + col] = __uint_as_float(d1.x);
@@ -567,7 +572,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         }
 #pragma unroll
         for (int j = 0; j < TN; j += 2) {
-          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(pBv + kp * BN + tx * TN + j);
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(pBv + kp * BN + b_slot(tx * TN + j));
           b2[j] = v.x;
           b2[j + 1] = v.y;
         }

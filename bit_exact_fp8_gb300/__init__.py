@@ -9,7 +9,9 @@ The C ABI is include/emu_fp8.h (libemufp8.so, built by ``build.build()``);
 ``_lib`` binds it through ctypes, ``api`` adds the torch-facing call.
 """
 from .api import (EmuCudaError, EmuError, ReferenceRejectsError, UnsupportedFeatureError,
-                  accumulate, preset_params, scaled_mm, workspace_bytes)
+                  accumulate, preset_params, scaled_mm, scaled_mm_host, staging_bytes,
+                  workspace_bytes)
 
-__all__ = ["scaled_mm", "accumulate", "preset_params", "workspace_bytes", "EmuError",
-           "ReferenceRejectsError", "UnsupportedFeatureError", "EmuCudaError"]
+__all__ = ["scaled_mm", "scaled_mm_host", "accumulate", "preset_params", "workspace_bytes",
+           "staging_bytes", "EmuError", "ReferenceRejectsError", "UnsupportedFeatureError",
+           "EmuCudaError"]

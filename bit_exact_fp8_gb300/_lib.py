@@ -26,7 +26,8 @@ EMU_OUT_E5M2 = 4
 #: every symbol include/emu_fp8.h declares
 EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
             "emu_abi_version", "emu_scaled_mm_noalloc", "emu_device_status",
-            "emu_selftest_wait_timeout", "emu_scaled_mm_ex")
+            "emu_selftest_wait_timeout", "emu_scaled_mm_ex", "emu_host_staging_bytes",
+            "emu_scaled_mm_host")
 
 #: size of the static scratch of emu_scaled_mm_noalloc (EMU_NOALLOC_SCRATCH_BYTES)
 EMU_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -73,6 +74,15 @@ def load(path: str = LIB) -> ctypes.CDLL:
                                         ctypes.c_int32, ctypes.c_int32,
                                         ctypes.POINTER(emu_preset_t), P]
     L.emu_scaled_mm_noalloc.restype = ctypes.c_int
+    L.emu_host_staging_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.c_int32, ctypes.c_int]
+    L.emu_host_staging_bytes.restype = ctypes.c_size_t
+    L.emu_scaled_mm_host.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                     ctypes.c_float, P, P, ctypes.c_int, ctypes.c_int32,
+                                     ctypes.c_int32, ctypes.POINTER(emu_preset_t), P,
+                                     ctypes.c_size_t, ctypes.c_int32, P]
+    L.emu_scaled_mm_host.restype = ctypes.c_int
     L.emu_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
     L.emu_device_status.restype = ctypes.c_int
     L.emu_selftest_wait_timeout.argtypes = [P]
@@ -126,6 +136,26 @@ def emu_scaled_mm_noalloc(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int
         ctypes.c_void_p(A), fmt_a, ctypes.c_void_p(B), fmt_b, M, N, K,
         ctypes.c_void_p(scale_a), ctypes.c_void_p(scale_b), ctypes.c_void_p(out), out_dtype,
         int(fast_accum), int(split_S), ctypes.byref(preset), ctypes.c_void_p(stream)))
+
+
+def emu_host_staging_bytes(M: int, N: int, K: int, split_S: int, out_dtype: int) -> int:
+    return int(load().emu_host_staging_bytes(M, N, K, split_S, out_dtype))
+
+
+def emu_scaled_mm_host(A_host: int, fmt_a: int, B_host: int, fmt_b: int, M: int, N: int, K: int,
+                       scale_a: float, scale_b: float, scale_result, out_host: int,
+                       out_dtype: int, fast_accum: int, split_S: int, preset: emu_preset_t,
+                       staging: int, staging_bytes: int, chunks: int, stream: int) -> int:
+    """The C call with host operand/result addresses and a device staging buffer
+    (ints); scale_result is None or a float (passed by host pointer).  Asynchronous:
+    the result is in out_host once `stream` completes.  Returns the status code."""
+    sr = None if scale_result is None else ctypes.c_float(float(scale_result))
+    return int(load().emu_scaled_mm_host(
+        ctypes.c_void_p(A_host), fmt_a, ctypes.c_void_p(B_host), fmt_b, M, N, K,
+        float(scale_a), float(scale_b), None if sr is None else ctypes.byref(sr),
+        ctypes.c_void_p(out_host), out_dtype, int(fast_accum), int(split_S),
+        ctypes.byref(preset), ctypes.c_void_p(staging), int(staging_bytes), int(chunks),
+        ctypes.c_void_p(stream)))
 
 
 def emu_device_status(reset: bool = False) -> int:

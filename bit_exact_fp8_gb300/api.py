@@ -128,6 +128,66 @@ def scaled_mm(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
     return out
 
 
+def staging_bytes(M: int, N: int, K: int, split_S: int, out_dtype: torch.dtype) -> int:
+    """Device staging bytes scaled_mm_host needs for these sizes."""
+    return _lib.emu_host_staging_bytes(M, N, K, split_S, _OUT[out_dtype])
+
+
+def scaled_mm_host(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: float, scale_b: float,
+                   scale_result: Optional[float] = None, out_dtype: Optional[torch.dtype] = None,
+                   use_fast_accum: bool = False, *, splitk: int = 1, preset="hopper",
+                   out: Optional[torch.Tensor] = None, staging: Optional[torch.Tensor] = None,
+                   chunks: int = 0, device=None, synchronize: bool = True) -> torch.Tensor:
+    """``scaled_mm`` on HOST tensors: mat1 [M,K] row-major and mat2 [K,N]
+    column-major FP8 tensors in host memory (pinned, e.g. ``.pin_memory()``, for
+    the copies to overlap the compute), scales as Python floats.  The library
+    uploads the operands in ``chunks`` column slabs (0: one per 64 MiB of B),
+    computes each slab as soon as it has landed and copies the result back, on its own streams ordered after the
+    current stream of ``device``; the bits equal those of ``scaled_mm``.  Returns
+    the host [M,N] result (``out`` if given, pinned); with ``synchronize=False`` it
+    is valid only once the device's current stream has completed."""
+    if mat1.dim() != 2 or mat2.dim() != 2:
+        raise ValueError("mat1 and mat2 must be 2-D")
+    if mat1.dtype not in _FMT or mat2.dtype not in _FMT:
+        raise ReferenceRejectsError(f"FP8 operands expected, got {mat1.dtype}, {mat2.dtype}")
+    if mat1.is_cuda or mat2.is_cuda:
+        raise ValueError("scaled_mm_host takes host tensors (use scaled_mm for device tensors)")
+    M, K = mat1.shape
+    K2, N = mat2.shape
+    if K != K2:
+        raise ValueError(f"shape mismatch: {tuple(mat1.shape)} @ {tuple(mat2.shape)}")
+    if mat1.numel() > 0 and not mat1.is_contiguous():
+        raise ReferenceRejectsError("mat1 must be row-major")
+    if mat2.numel() > 0 and not (mat2.stride(0) == 1 and (mat2.stride(1) == K or N <= 1)):
+        raise ReferenceRejectsError("mat2 must be column-major ([K, N] with K contiguous, e.g. w.t())")
+    if out_dtype is None:
+        out_dtype = mat1.dtype
+    if out_dtype not in _OUT:
+        raise UnsupportedFeatureError(f"out_dtype {out_dtype} is not supported")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    P = preset_params(preset)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, pin_memory=True)
+    elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous() or out.is_cuda:
+        raise ValueError("out must be a contiguous host [M, N] tensor of out_dtype")
+    need = _lib.emu_host_staging_bytes(M, N, K, int(splitk), _OUT[out_dtype])
+    if staging is None or staging.numel() * staging.element_size() < need or staging.data_ptr() % 256:
+        staging = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        st = _lib.emu_scaled_mm_host(mat1.data_ptr(), _FMT[mat1.dtype], mat2.data_ptr(),
+                                     _FMT[mat2.dtype], M, N, K, scale_a, scale_b, scale_result,
+                                     out.data_ptr(), _OUT[out_dtype], int(bool(use_fast_accum)),
+                                     int(splitk), P, staging.data_ptr(),
+                                     staging.numel() * staging.element_size(), int(chunks),
+                                     stream.cuda_stream)
+        if st != _lib.EMU_OK:
+            _raise(st, "emu_scaled_mm_host")
+        if synchronize:
+            stream.synchronize()
+    return out
+
+
 def accumulate(x: torch.Tensor, w: torch.Tensor, use_fast_accum: bool, *, splitk: int = 1,
                preset="hopper") -> torch.Tensor:
     """The fp32 accumulator before the scales ("User guide", section 3: both operands

@@ -290,19 +290,21 @@ int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t
                           fast_accum, split_S, preset, workspace, workspace_bytes, stream);
 }
 
-int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,
-                     int64_t M, int64_t N, int64_t K, const float* scale_a, const float* scale_b,
-                     const float* scale_result, void* out, emu_out_t out_dtype,
-                     int32_t fast_accum, int32_t split_S, const emu_preset_t* preset,
-                     void* workspace, size_t workspace_bytes, void* stream) {
-  g_last_error.clear();
+}  // extern "C"
+
+namespace {
+
+// The checks every entry point shares: formats, output dtype, sizes, preset.
+int check_args(emu_fp8_t fmt_a, emu_fp8_t fmt_b, int64_t M, int64_t N, int64_t K,
+               bool has_scale_result, emu_out_t out_dtype, int32_t split_S,
+               const emu_preset_t* preset) {
   if (!preset) return fail(EMU_EINVAL, "preset is null");
   if ((int)fmt_a < 0 || (int)fmt_a > 1 || (int)fmt_b < 0 || (int)fmt_b > 1)
     return fail(EMU_EINVAL, "unknown FP8 format (%d, %d)", (int)fmt_a, (int)fmt_b);
   if ((int)out_dtype < 0 || (int)out_dtype > 4)
     return fail(EMU_EINVAL, "unknown output dtype %d", (int)out_dtype);
   const bool fp8_out = out_dtype == EMU_OUT_E4M3FN || out_dtype == EMU_OUT_E5M2;
-  if (scale_result && !fp8_out)
+  if (has_scale_result && !fp8_out)
     return fail(EMU_EUNSUPPORTED, "scale_result applies to fp8 outputs only");
   if (fmt_a == EMU_E4M3FN && fmt_b == EMU_E4M3FN && out_dtype == EMU_OUT_E5M2)
     return fail(EMU_EREJECT, "cuBLASLt refuses e4m3 x e4m3 -> e5m2");
@@ -333,6 +335,214 @@ int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp
     return fail(EMU_EUNSUPPORTED, "ktile %d must be a positive multiple of 32", preset->ktile);
   if (preset->combine != 0 && preset->combine != 1)
     return fail(EMU_EINVAL, "combine %d", preset->combine);
+  return EMU_OK;
+}
+
+// Enqueue the GEMM of checked, device-resident arguments on `st`: the K == 0 fill,
+// or the tile kernel and, for S > 1, the combine kernel.
+int enqueue(const emu::GemmParams& p, const emu_preset_t* preset, int32_t fast_accum,
+            cudaStream_t st) {
+  if (p.K == 0) {
+    const int64_t MN = p.M * p.N;
+    const int threads = 256;
+    const int64_t blocks = (MN + threads - 1) / threads;
+    emu::emu_fill_k0_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(p);
+  } else {
+    const int rc = launch_gemm(p, preset->block_width, fast_accum == 0, st);
+    if (rc != EMU_OK) return rc;
+    if (p.S > 1) {
+      const int64_t MN = p.M * p.N;
+      const int threads = 256;
+      const int64_t blocks = (MN + threads - 1) / threads;
+      emu::emu_combine_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(
+          p, preset->combine);
+    }
+  }
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(EMU_ECUDA, "CUDA launch failed: %s", cudaGetErrorString(e));
+  return EMU_OK;
+}
+
+emu::GemmParams make_params(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,
+                            int64_t M, int64_t N, int64_t K, const float* scale_a,
+                            const float* scale_b, const float* scale_result, void* out,
+                            emu_out_t out_dtype, int32_t split_S, const emu_preset_t* preset,
+                            void* workspace) {
+  emu::GemmParams p;
+  p.A = A; p.B = B; p.M = M; p.N = N; p.K = K;
+  p.fmt_a = (int)fmt_a; p.fmt_b = (int)fmt_b;
+  p.scale_a = scale_a; p.scale_b = scale_b;
+  p.out = out; p.out_dtype = (int)out_dtype;
+  p.scale_result = scale_result;
+  p.partial = static_cast<float*>(workspace);
+  p.S = split_S; p.scheme = preset->split_scheme; p.ktile = preset->ktile;
+  p.restart_blocks = preset->restart / preset->block_width;
+  return p;
+}
+
+// ---- host-buffer pipeline (emu_scaled_mm_host)
+constexpr int kHostMaxChunks = 16;
+constexpr int kHostComputeStreams = 4;
+
+// Streams and events of one device, created on first use and kept for the process.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaStream_t comp[kHostComputeStreams] = {};
+  cudaEvent_t entry = nullptr, done = nullptr;
+  cudaEvent_t uploaded[kHostMaxChunks] = {}, computed[kHostMaxChunks] = {};
+};
+std::mutex g_host_mu;            // one host thread enqueues at a time
+HostPipe g_host_pipe[64];
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(EMU_ECUDA, "no current CUDA device");
+  HostPipe& hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    bool ok = cudaStreamCreateWithFlags(&hp.up, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kHostComputeStreams; ++i)
+      ok = cudaStreamCreateWithFlags(&hp.comp[i], cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; ok && i < kHostMaxChunks; ++i)
+      ok = cudaEventCreateWithFlags(&hp.uploaded[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.computed[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return fail(EMU_ECUDA, "creating the copy streams failed: %s",
+                         cudaGetErrorString(cudaGetLastError()));
+    hp.ready = true;
+  }
+  *out = &hp;
+  return EMU_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t out_elem_bytes(emu_out_t t) {
+  return t == EMU_OUT_F32 ? 4 : (t == EMU_OUT_BF16 || t == EMU_OUT_F16) ? 2 : 1;
+}
+
+// staging buffer: scalars | A [M,K] | B [N,K] | out [M,N] | split partials [S,M,N] f32,
+// each region starting on a 256-byte boundary
+struct StagingLayout {
+  size_t a, b, out, part, total;
+};
+StagingLayout staging_layout(int64_t M, int64_t N, int64_t K, int32_t S, emu_out_t od) {
+  StagingLayout l;
+  l.a = 256;
+  l.b = l.a + round256((size_t)M * (size_t)K);
+  l.out = l.b + round256((size_t)N * (size_t)K);
+  l.part = l.out + round256((size_t)M * (size_t)N * out_elem_bytes(od));
+  l.total = l.part + (S > 1 ? round256((size_t)S * (size_t)M * (size_t)N * 4) : 0);
+  return l;
+}
+
+#define EMU_CK(call)                                                                      \
+  do {                                                                                    \
+    const cudaError_t e_ = (call);                                                        \
+    if (e_ != cudaSuccess) return fail(EMU_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+size_t emu_host_staging_bytes(int64_t M, int64_t N, int64_t K, int32_t split_S,
+                              emu_out_t out_dtype) {
+  if (M < 0 || N < 0 || K < 0 || split_S < 1 || (int)out_dtype < 0 || (int)out_dtype > 4) return 0;
+  return staging_layout(M, N, K, split_S, out_dtype).total;
+}
+
+int emu_scaled_mm_host(const uint8_t* A_host, emu_fp8_t fmt_a, const uint8_t* B_host,
+                       emu_fp8_t fmt_b, int64_t M, int64_t N, int64_t K, float scale_a,
+                       float scale_b, const float* scale_result, void* out_host,
+                       emu_out_t out_dtype, int32_t fast_accum, int32_t split_S,
+                       const emu_preset_t* preset, void* staging, size_t staging_bytes,
+                       int32_t chunks, void* stream) {
+  g_last_error.clear();
+  int rc = check_args(fmt_a, fmt_b, M, N, K, scale_result != nullptr, out_dtype, split_S, preset);
+  if (rc != EMU_OK) return rc;
+  if (M == 0 || N == 0) return EMU_OK;
+  if (!out_host) return fail(EMU_EINVAL, "null out_host");
+  if (K > 0 && (!A_host || !B_host)) return fail(EMU_EINVAL, "null operand pointer");
+  const StagingLayout lay = staging_layout(M, N, K, split_S, out_dtype);
+  if (!staging || staging_bytes < lay.total)
+    return fail(EMU_EINVAL, "staging of %zu bytes needed (got %zu)", lay.total, staging_bytes);
+  if ((reinterpret_cast<uintptr_t>(staging) & 255u) != 0)
+    return fail(EMU_EINVAL, "staging must be 256-byte aligned");
+  // default: one slab per 64 MiB of B (each copy costs tens of microseconds of setup)
+  int nch = chunks > 0 ? chunks : (int)(1 + ((size_t)N * (size_t)K >> 26));
+  if (nch > kHostMaxChunks) nch = kHostMaxChunks;
+  if (nch > N / 16) nch = (int)(N / 16);
+  auto slab = [&](int c) { return (int64_t)((N / 16) * c / nch) * 16; };   // column start
+  const size_t esz = out_elem_bytes(out_dtype);
+  unsigned char* base = static_cast<unsigned char*>(staging);
+  float* scal = reinterpret_cast<float*>(base);
+  const uint8_t* dA = base + lay.a;
+  unsigned char* dB = base + lay.b;
+  unsigned char* dOut = base + lay.out;
+  float* dPart = reinterpret_cast<float*>(base + lay.part);
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(&hp);
+  if (rc != EMU_OK) return rc;
+  cudaGetLastError();   // clear a stale launch error of an earlier call
+  EMU_CK(cudaEventRecord(hp->entry, user));
+  EMU_CK(cudaStreamWaitEvent(hp->up, hp->entry, 0));
+  EMU_CK(cudaStreamWaitEvent(hp->down, hp->entry, 0));
+  for (int i = 0; i < kHostComputeStreams; ++i) EMU_CK(cudaStreamWaitEvent(hp->comp[i], hp->entry, 0));
+  // upload: scalars, A, then B slab by slab
+  emu::emu_set_scalars_kernel<<<1, 32, 0, hp->up>>>(scal, scale_a, scale_b,
+                                                      scale_result ? *scale_result : 1.0f);
+  EMU_CK(cudaGetLastError());
+  if (K > 0) EMU_CK(cudaMemcpyAsync(base + lay.a, A_host, (size_t)M * (size_t)K,
+                                    cudaMemcpyHostToDevice, hp->up));
+  for (int c = 0; c < nch; ++c) {
+    const int64_t n0 = slab(c), n1 = slab(c + 1);
+    if (K > 0)
+      EMU_CK(cudaMemcpyAsync(dB + (size_t)n0 * (size_t)K, B_host + (size_t)n0 * (size_t)K,
+                             (size_t)(n1 - n0) * (size_t)K, cudaMemcpyHostToDevice, hp->up));
+    EMU_CK(cudaEventRecord(hp->uploaded[c], hp->up));
+  }
+  // compute: slab c on compute stream c mod 4, once its B slab has landed
+  for (int c = 0; c < nch; ++c) {
+    const int64_t n0 = slab(c), n1 = slab(c + 1);
+    cudaStream_t cs = hp->comp[c % kHostComputeStreams];
+    EMU_CK(cudaStreamWaitEvent(cs, hp->uploaded[c], 0));
+    const emu::GemmParams p = make_params(
+        dA, fmt_a, dB + (size_t)n0 * (size_t)K, fmt_b, M, n1 - n0, K, scal, scal + 1,
+        scale_result ? scal + 2 : nullptr, dOut + (size_t)M * (size_t)n0 * esz, out_dtype, split_S,
+        preset, split_S > 1 ? dPart + (size_t)split_S * (size_t)M * (size_t)n0 : nullptr);
+    rc = enqueue(p, preset, fast_accum, cs);
+    if (rc != EMU_OK) return rc;
+    EMU_CK(cudaEventRecord(hp->computed[c], cs));
+  }
+  // download: each finished slab into its columns of out_host
+  for (int c = 0; c < nch; ++c) {
+    const int64_t n0 = slab(c), n1 = slab(c + 1);
+    EMU_CK(cudaStreamWaitEvent(hp->down, hp->computed[c], 0));
+    EMU_CK(cudaMemcpy2DAsync(static_cast<unsigned char*>(out_host) + (size_t)n0 * esz,
+                             (size_t)N * esz, dOut + (size_t)M * (size_t)n0 * esz,
+                             (size_t)(n1 - n0) * esz, (size_t)(n1 - n0) * esz, (size_t)M,
+                             cudaMemcpyDeviceToHost, hp->down));
+  }
+  EMU_CK(cudaEventRecord(hp->done, hp->down));
+  EMU_CK(cudaStreamWaitEvent(user, hp->done, 0));
+  return EMU_OK;
+}
+
+int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,
+                     int64_t M, int64_t N, int64_t K, const float* scale_a, const float* scale_b,
+                     const float* scale_result, void* out, emu_out_t out_dtype,
+                     int32_t fast_accum, int32_t split_S, const emu_preset_t* preset,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int rc = check_args(fmt_a, fmt_b, M, N, K, scale_result != nullptr, out_dtype, split_S, preset);
+  if (rc != EMU_OK) return rc;
   if (M == 0 || N == 0) return EMU_OK;
   if (!out || !scale_a || !scale_b) return fail(EMU_EINVAL, "null out or scale pointer");
   if (K > 0 && (!A || !B)) return fail(EMU_EINVAL, "null operand pointer");
@@ -344,38 +554,10 @@ int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp
       return fail(EMU_EINVAL, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
     if (!aligned16(workspace)) return fail(EMU_EINVAL, "workspace must be 16-byte aligned");
   }
-
-  emu::GemmParams p;
-  p.A = A; p.B = B; p.M = M; p.N = N; p.K = K;
-  p.fmt_a = (int)fmt_a; p.fmt_b = (int)fmt_b;
-  p.scale_a = scale_a; p.scale_b = scale_b;
-  p.out = out; p.out_dtype = (int)out_dtype;
-  p.scale_result = scale_result;
-  p.partial = static_cast<float*>(workspace);
-  p.S = split_S; p.scheme = preset->split_scheme; p.ktile = preset->ktile;
-  p.restart_blocks = preset->restart / preset->block_width;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
+  const emu::GemmParams p = make_params(A, fmt_a, B, fmt_b, M, N, K, scale_a, scale_b,
+                                        scale_result, out, out_dtype, split_S, preset, workspace);
   cudaGetLastError();   // clear a stale launch error of an earlier call
-  if (K == 0) {
-    const int64_t MN = M * N;
-    const int threads = 256;
-    const int64_t blocks = (MN + threads - 1) / threads;
-    emu::emu_fill_k0_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(p);
-  } else {
-    const int rc = launch_gemm(p, preset->block_width, fast_accum == 0, st);
-    if (rc != EMU_OK) return rc;
-    if (split_S > 1) {
-      const int64_t MN = M * N;
-      const int threads = 256;
-      const int64_t blocks = (MN + threads - 1) / threads;
-      emu::emu_combine_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), threads, 0, st>>>(
-          p, preset->combine);
-    }
-  }
-  const cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(EMU_ECUDA, "CUDA launch failed: %s", cudaGetErrorString(e));
-  return EMU_OK;
+  return enqueue(p, preset, fast_accum, static_cast<cudaStream_t>(stream));
 }
 
 int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,

@@ -769,6 +769,16 @@ __global__ void emu_wait_timeout_selftest_kernel(uint32_t polls) {
   }
 }
 
+// Three fp32 scalars into device memory (the host-buffer entry point's scales),
+// taken as launch arguments so that no host buffer has to outlive the call
+__global__ void emu_set_scalars_kernel(float* dst, float a, float b, float c) {
+  if (threadIdx.x == 0) {
+    dst[0] = a;
+    dst[1] = b;
+    dst[2] = c;
+  }
+}
+
 // K == 0: every output is fma(+0, alpha, +0)
 __global__ void emu_fill_k0_kernel(const GemmParams p) {
   const int64_t MN = p.M * p.N;

@@ -182,6 +182,54 @@ int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a,
                           void* stream);
 
 /*
+ * emu_scaled_mm_host: the same GEMM with the operands and the result in HOST memory,
+ * the copies overlapped with the compute.  (An addition of this library; the pages
+ * have no counterpart: they describe the arithmetic, not the data movement.)
+ *
+ * N is cut into `chunks` column slabs (widths multiples of 16; chunks <= 0 picks
+ * one slab per 64 MiB of B; never more than 16 slabs, nor more than N / 16).  One stream copies the scales, A and then B
+ * slab by slab into the device staging buffer; each slab's GEMM starts on one of
+ * four compute streams as soon as its B slab has landed, so slab c + 1 uploads
+ * while slab c computes; a third stream copies each finished slab of the result
+ * back into its columns of out_host (a strided 2-D copy).  Every output depends
+ * only on its row of A and column of B, so the bits equal those of one
+ * emu_scaled_mm_ex call on the whole problem.
+ *
+ *   A_host, B_host  host, layouts as in emu_scaled_mm (B: [N,K] bytes, n-major)
+ *   scale_a/b       the fp32 scales by value
+ *   scale_result    host pointer to one fp32 (FP8 outputs), or NULL
+ *   out_host        host, [M,N] row-major, element type out_dtype
+ *   staging         device buffer of at least emu_host_staging_bytes(M, N, K,
+ *                   split_S, out_dtype) bytes, 256-byte aligned; scratch only
+ *   chunks          number of column slabs (<= 0: one per 64 MiB of B)
+ *   stream          the caller's stream: the work starts after what the stream
+ *                   holds at the call, and the stream waits for the last copy back
+ *
+ * Asynchronous: the call returns once everything is enqueued; out_host holds the
+ * result when `stream` has completed, and the host buffers must stay valid and
+ * unchanged until then.  Pinned host memory (cudaHostAlloc / pin_memory) lets the
+ * copies overlap the compute; pageable memory works, without the overlap.  Calls
+ * issued on different caller streams with different staging buffers overlap one
+ * call's uploads with another's GEMM.  The
+ * call keeps no pointer after the stream completes.  Status codes and argument
+ * checks are those of emu_scaled_mm_ex; EMU_EINVAL also for a short or misaligned
+ * staging buffer; EMU_ECUDA when a copy or a stream operation fails.  Calls from
+ * several host threads are serialised while they enqueue.
+ */
+size_t emu_host_staging_bytes(int64_t M, int64_t N, int64_t K, int32_t split_S,
+                              emu_out_t out_dtype);
+
+int emu_scaled_mm_host(const uint8_t* A_host, emu_fp8_t fmt_a,
+                       const uint8_t* B_host, emu_fp8_t fmt_b,
+                       int64_t M, int64_t N, int64_t K,
+                       float scale_a, float scale_b, const float* scale_result,
+                       void* out_host, emu_out_t out_dtype,
+                       int32_t fast_accum, int32_t split_S,
+                       const emu_preset_t* preset,
+                       void* staging, size_t staging_bytes,
+                       int32_t chunks, void* stream);
+
+/*
  * Device status of the library on the current device: *status = 0, or 1 when a
  * kernel's wait for its TMA loads gave up (each wait polls a bounded number of
  * times instead of hanging; the CTA then returns early and the outputs of that

@@ -142,3 +142,53 @@ def test_fp8_output_argument_checks(lib):
     assert ex(0, 0, 1, FAKE) == -3       # scale_result with a non-fp8 output
     assert ex(0, 0, 5, 0) == -1          # unknown output dtype
     assert L is not None
+
+
+def test_host_staging_bytes(lib):
+    # scalars (256) | A | B | out | partials, each rounded up to 256 bytes
+    r = lambda x: (x + 255) // 256 * 256
+    M, N, K = 64, 5760, 1920
+    assert lib.emu_host_staging_bytes(M, N, K, 1, lib.EMU_OUT_BF16) == \
+        256 + r(M * K) + r(N * K) + r(M * N * 2)
+    assert lib.emu_host_staging_bytes(16, 256, 4096, 8, lib.EMU_OUT_F32) == \
+        256 + r(16 * 4096) + r(256 * 4096) + r(16 * 256 * 4) + r(8 * 16 * 256 * 4)
+    assert lib.emu_host_staging_bytes(3, 16, 32, 1, lib.EMU_OUT_E4M3FN) == 256 + 256 + 512 + 256
+    assert lib.emu_host_staging_bytes(-1, 16, 32, 1, 0) == 0
+    assert lib.emu_host_staging_bytes(1, 16, 32, 0, 0) == 0
+    assert lib.emu_host_staging_bytes(1, 16, 32, 1, 5) == 0
+
+
+def test_host_entry_point_argument_errors(lib):
+    # every case fails its checks before any CUDA call (no GPU here)
+    p = lib.emu_preset_get("hopper")
+    need = lib.emu_host_staging_bytes(16, 64, 256, 1, lib.EMU_OUT_BF16)
+
+    def host(**kw):
+        a = dict(A=FAKE, fa=0, B=FAKE, fb=0, M=16, N=64, K=256, sa=1.0, sb=1.0, sr=None,
+                 out=FAKE, od=lib.EMU_OUT_BF16, fast=1, S=1, staging=1 << 20,
+                 staging_bytes=need, chunks=4)
+        a.update(kw)
+        return lib.emu_scaled_mm_host(a["A"], a["fa"], a["B"], a["fb"], a["M"], a["N"], a["K"],
+                                      a["sa"], a["sb"], a["sr"], a["out"], a["od"], a["fast"],
+                                      a["S"], p, a["staging"], a["staging_bytes"], a["chunks"], 0)
+    assert host(fa=1, fb=1) == lib.EMU_EREJECT                  # e5m2 x e5m2
+    assert host(od=lib.EMU_OUT_E5M2) == lib.EMU_EREJECT         # e4m3 x e4m3 -> e5m2
+    assert host(sr=2.0) == lib.EMU_EUNSUPPORTED                 # scale_result, bf16 out
+    assert host(N=40) == lib.EMU_EREJECT                        # N not a multiple of 16
+    assert host(S=0) == lib.EMU_EINVAL
+    assert host(out=0) == lib.EMU_EINVAL                        # null out_host
+    assert host(A=0) == lib.EMU_EINVAL                          # null operand
+    assert host(staging_bytes=need - 1) == lib.EMU_EINVAL       # short staging
+    assert "staging" in lib.emu_last_error()
+    assert host(staging=(1 << 20) + 16) == lib.EMU_EINVAL       # not 256-byte aligned
+    assert host(M=0, A=0, B=0, out=0, staging=0, staging_bytes=0) == lib.EMU_OK   # no-op
+
+
+def test_python_host_api_rejects_device_and_bad_dtypes():
+    from bit_exact_fp8_gb300 import ReferenceRejectsError, scaled_mm_host
+    x = torch.zeros(16, 32).to(torch.float8_e4m3fn)
+    w = torch.zeros(16, 32).to(torch.float8_e4m3fn)
+    with pytest.raises(ReferenceRejectsError):
+        scaled_mm_host(x.float(), w.t(), 1.0, 1.0)
+    with pytest.raises(ValueError):
+        scaled_mm_host(x, w, 1.0, 1.0)                          # [16,32] @ [16,32]

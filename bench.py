@@ -44,6 +44,7 @@ UNIT = "TFLOP/s"
 SMS = 152
 LANES_PER_SM = 128          # 4 sub-partitions x 32 lanes: one warp instruction per clock each
 OPS_PER_MAC = 5             # exponent add, max, significand multiply, align shift, add
+FP32_OPS_PER_MAC = 3        # the kernel's exact product, truncating multiply and exact add
 
 
 def measured_peaks():
@@ -311,6 +312,11 @@ def run_gpu(args, cs):
             "note": f"{OPS_PER_MAC} lane-ops per MAC (algorithmic); peak = {SMS} SMs x "
                     f"{LANES_PER_SM} lanes x {mhz:.0f} MHz issue slots (recipe unit counts, "
                     "sm_max_mhz of MEASURED_PEAKS.json)"}
+    # this implementation's own ceiling: pass 2 issues packed f32x2 instructions, so the
+    # FP32 pipe (128 operations per clock per SM) bounds it at 3 FP32 operations per MAC
+    roof["fp32_pipe"] = {"ops_per_mac": FP32_OPS_PER_MAC, "peak": peak,
+                         "achieved": FP32_OPS_PER_MAC * achieved / OPS_PER_MAC,
+                         "frac": FP32_OPS_PER_MAC * achieved / OPS_PER_MAC / peak}
     if peaks and "hbm_gbs" in peaks:
         bytes_step = cs.M * cs.K + cs.N * cs.K + cs.M * cs.N * (4 if cs.out_dtype == "f32" else 2)
         roof["hbm_gbs"] = bytes_step / (t_sum / args.steps) / 1e9

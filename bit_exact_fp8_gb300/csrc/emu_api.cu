@@ -36,11 +36,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Tile shapes (thread tile TM x TN, CTA WM x WN threads, K-stage BK); "packed": the
 // pass-2 products, truncations and sums run as f32x2 pairs of adjacent k:
-//   M40  4 x 2, 16 x 20 threads, BK 64:  64 x 40 outputs per CTA, packed (M <= 64 with
-//        wide N: one CTA per SM)
+//   M40  4 x 2, 16 x 20 threads, BK 128: 64 x 40 outputs per CTA, packed (M <= 64 with
+//        wide N: one CTA per SM, so the long stage halves the per-stage barriers)
 //   M32  4 x 4, 16 x  8 threads, BK 32:  64 x 32, packed, three CTAs per SM
 //   M64  4 x 4, 16 x 16 threads, BK 32:  64 x 64, packed, two CTAs per SM (slow: one)
-//   S    2 x 2,  8 x 16 threads, BK 32:  16 x 32, packed (skinny, split-K)
+//   S    2 x 2,  8 x 16 threads, BK 64:  16 x 32, packed (skinny, split-K)
 //   K8   1 x 2,  4 x  4 x 8 lanes, BK 64:  4 x  8, each block split over 8 lanes
 //   K4   1 x 2,  4 x  8 x 4 lanes, BK 64:  4 x 16, each block split over 4 lanes
 //   K8H, K4H: the same with BK 128, so a stage's barrier and wait are shared by four
@@ -64,9 +64,9 @@ struct TileInfo {
 // resident is also the kernel's __launch_bounds__ minimum, which holds ptxas to
 // 65536 / (resident * threads) registers
 constexpr TileInfo kTiles[] = {
-    {"M40", 4, 2, 64, 40, 320, 1, 1, 64, 1, 7.2, 150.0, 1.0, -1},
+    {"M40", 4, 2, 64, 40, 320, 1, 1, 128, 1, 6.7, 140.0, 1.0, -1},
     {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 5.3, 200.0, 1.0, -1},
-    {"S", 2, 2, 16, 32, 128, 4, 4, 32, 1, 8.0, 63.0, 1.0, -1},
+    {"S", 2, 2, 16, 32, 128, 4, 4, 64, 1, 8.0, 55.0, 1.0, -1},
     {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 51.0, 35.0, 1.0, 6},
     {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 38.0, 38.4, 1.0, 7},
     {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, -1},
@@ -133,11 +133,10 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_
   return EMU_OK;
 }
 
-template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, bool DUAL, int G, int MINB,
-          bool PK>
+template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, int G, int MINB, bool PK>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, DUAL, G, MINB, PK>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK>;
   // the dynamic shared memory limit is a per-function, per-device attribute
   static bool configured[64] = {false};
   int dev = 0;
@@ -159,15 +158,15 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
 
 // MINB, MINB_SLOW: the CTAs per SM the fast and slow variants are meant to keep
 // resident (the register budget ptxas is held to)
-template <int TM, int TN, int WM, int WN, int BK, bool DUAL, int G, int MINB, int MINB_SLOW = MINB,
+template <int TM, int TN, int WM, int WN, int BK, int G, int MINB, int MINB_SLOW = MINB,
           bool PK = true>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, DUAL, G, MINB_SLOW, PK>(p, st)
-                : launch_one<TM, TN, WM, WN, BK, 32, false, DUAL, G, MINB, PK>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, G, MINB_SLOW, PK>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, G, MINB, PK>(p, st);
   }
-  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, DUAL, G, MINB_SLOW, PK>(p, st)
-              : launch_one<TM, TN, WM, WN, BK, 16, false, DUAL, G, MINB, PK>(p, st);
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, G, MINB_SLOW, PK>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK>(p, st);
 }
 
 // Pick the tile with the lowest estimated time per K element, in SM clocks: the
@@ -207,14 +206,14 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   switch (choose_tile(p, slow)) {
-    case 0: return launch_tile<4, 2, 16, 20, 64, true, 1, 1>(p, blk, slow, st);
-    case 1: return launch_tile<4, 4, 16, 8, 32, false, 1, 3>(p, blk, slow, st);
-    case 2: return launch_tile<2, 2, 8, 16, 32, true, 1, 4>(p, blk, slow, st);
-    case 3: return launch_tile<1, 2, 4, 4, 64, false, 8, 8, 8, false>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 8, 64, false, 4, 8, 8, false>(p, blk, slow, st);
-    case 5: return launch_tile<4, 4, 16, 16, 32, false, 1, 2, 1>(p, blk, slow, st);
-    case 6: return launch_tile<1, 2, 4, 4, 128, false, 8, 7, 7, false>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 128, false, 4, 4, 4, false>(p, blk, slow, st);
+    case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1>(p, blk, slow, st);
+    case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3>(p, blk, slow, st);
+    case 2: return launch_tile<2, 2, 8, 16, 64, 1, 4>(p, blk, slow, st);
+    case 3: return launch_tile<1, 2, 4, 4, 64, 8, 8, 8, false>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 8, 64, 4, 8, 8, false>(p, blk, slow, st);
+    case 5: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, 8, 7, 7, false>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 128, 4, 4, 4, false>(p, blk, slow, st);
   }
 }
 

@@ -273,9 +273,9 @@ __device__ __forceinline__ uint32_t c16_hi(float c) { return __float_as_uint(c) 
 // The GEMM kernel.  Thread tile TM x TN outputs; CTA WM x WN threads; K staged in
 // steps of BK_ (32, 64 or 128) codes through two shared-memory buffers, so one
 // barrier per stage suffices; BLK products per block (16 or 32); SLOW: restart
-// chunks; DUAL: two partial sums per output in pass 2 (the terms are exact multiples
-// of 2^-149, so any association gives the same sum); PK: pass 2 on packed f32x2
-// k-pairs.  G > 1 ("lane split", for skinny shapes with few, long chains): G
+// chunks; PK: pass 2 on packed f32x2 k-pairs, whose two halves are two partial sums
+// of the block (the terms are exact multiples of 2^-149, so any association gives
+// the same sum).  G > 1 ("lane split", for skinny shapes with few, long chains): G
 // adjacent lanes share one thread tile and take every G-th k-pair (pass 1) and
 // product (pass 2) of each block; their partial block maxima and partial sums are
 // combined with warp shuffles (exact), so all G lanes hold the same chain state.
@@ -314,7 +314,7 @@ struct TileShape {
   static_assert(RAW_A % RAW_ALIGN == 0, "the B box of a slot starts aligned");
 };
 
-template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, bool DUAL, int G, int MINB,
+template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, int G, int MINB,
           bool PK>
 __global__ void __launch_bounds__(WM * WN * G, MINB)
 emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
@@ -528,7 +528,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     // ---- scales 2^(-43-E) (as fp32 bit patterns) and the running sums: the high
     //      half takes max(even, odd, |c'|), clamped, and its exponent field
     uint32_t sc[TM][TN];
-    float acc[TM][TN], acc2[TM][TN];
+    float acc[TM][TN];
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -537,21 +537,18 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         const uint32_t e2 = __vmins2(__vmaxs2(m, c16_hi(cp[i][j])), kClampE2);
         sc[i][j] = kScaleBase - (e2 & 0x7F800000u);
         acc[i][j] = (G == 1 || gl == 0) ? fmul_rz(cp[i][j], __uint_as_float(sc[i][j])) : 0.0f;
-        acc2[i][j] = 0.0f;
       }
     // ---- pass 2: exact products, truncated onto the subnormal grid, summed exactly
     if constexpr (PK) {
       // on k-adjacent pairs: one packed multiply, multiply toward zero and add
-      // per two products; the two halves (and, with DUAL, two pair accumulators)
-      // are partial sums of the same exact terms
-      f32x2_t pa[TM][TN], pb[TM][TN], sc2[TM][TN];
+      // per two products; the two halves are partial sums of the same exact terms
+      f32x2_t pa[TM][TN], sc2[TM][TN];
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
         for (int j = 0; j < TN; ++j) {
           sc2[i][j] = pack2(__uint_as_float(sc[i][j]), __uint_as_float(sc[i][j]));
           pa[i][j] = pack2(acc[i][j], 0.0f);
-          pb[i][j] = 0ull;
         }
       const f32x2_t* pAv = reinterpret_cast<const f32x2_t*>(sAv);
       const f32x2_t* pBv = reinterpret_cast<const f32x2_t*>(sBv);
@@ -580,45 +577,29 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         for (int i = 0; i < TM; ++i)
 #pragma unroll
           for (int j = 0; j < TN; ++j) {
-            const f32x2_t t = fmul2_rz(fmul2_rn(a2[i], b2[j]), sc2[i][j]);
-            if (DUAL && (q & 1)) pb[i][j] = fadd2_rn(pb[i][j], t);
-            else pa[i][j] = fadd2_rn(pa[i][j], t);
+            pa[i][j] = fadd2_rn(pa[i][j], fmul2_rz(fmul2_rn(a2[i], b2[j]), sc2[i][j]));
           }
       }
 #pragma unroll
       for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) {
-          acc[i][j] = sum_halves(pa[i][j]);
-          if (DUAL) acc2[i][j] = sum_halves(pb[i][j]);
-        }
+        for (int j = 0; j < TN; ++j) acc[i][j] = sum_halves(pa[i][j]);
     } else {
       // one product at a time: this lane's products qG + gl
 #pragma unroll
       for (int q = 0; q < BLK / G; ++q) {
-        {
-          const int kk = q * G + gl;
-          float a[TM], b[TN];
+        const int kk = q * G + gl;
+        float a[TM], b[TN];
 #pragma unroll
-          for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ty * TM + i];
+        for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ty * TM + i];
 #pragma unroll
-          for (int j = 0; j < TN; ++j) b[j] = sBv[(k0 + kk) * BN + tx * TN + j];
+        for (int j = 0; j < TN; ++j) b[j] = sBv[(k0 + kk) * BN + tx * TN + j];
 #pragma unroll
-          for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) {
-              const float t = fmul_rz(fmul_rn(a[i], b[j]), __uint_as_float(sc[i][j]));
-              if (DUAL && (q & 1)) acc2[i][j] = fadd_rn(acc2[i][j], t);
-              else acc[i][j] = fadd_rn(acc[i][j], t);
-            }
-        }
+          for (int j = 0; j < TN; ++j)
+            acc[i][j] = fadd_rn(acc[i][j], fmul_rz(fmul_rn(a[i], b[j]), __uint_as_float(sc[i][j])));
       }
-    }
-    if (DUAL) {
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fadd_rn(acc[i][j], acc2[i][j]);
     }
     if (G > 1) {
 #pragma unroll

@@ -330,7 +330,14 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   constexpr int NBLK = BK / BLK;
   constexpr int A_CHUNKS = BM * BK / 16;
   constexpr int B_CHUNKS = BN * BK / 16;
-  constexpr int AB_PER = (A_CHUNKS + B_CHUNKS + NT - 1) / NT;
+  // Decoders.  Warp w issues from scheduler w % 4; with a warp count that is not a
+  // multiple of four, schedulers 0 .. NW % 4 - 1 hold one warp more, so only the warps
+  // on the others decode (the 10-warp linear tile: warps 2, 3, 6 and 7) and the busier
+  // schedulers carry compute alone.  Otherwise every thread decodes.
+  constexpr int NW = NT / 32;
+  constexpr int XW = NW % 4;
+  constexpr int NDEC = (XW == 0 || NW < 4 || NT % 32 != 0) ? NT : (NW / 4) * (4 - XW) * 32;
+  constexpr int AB_PER = (A_CHUNKS + B_CHUNKS + NDEC - 1) / NDEC;
   // packed B values: column n = tx * TN + j sits at pair slot (j / 2) * 2WN + 2tx + j % 2
   // of its k-pair row, so a thread's 16-byte loads of pairs (j, j + 1) are contiguous
   // across the warp's threads (the identity for TN = 2)
@@ -409,8 +416,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);   // label pairs
     float* sBv = reinterpret_cast<float*>(base + TS::B_VAL);
     uint32_t* sBl = reinterpret_cast<uint32_t*>(base + TS::B_LAB);   // label pairs
-    // A chunks first, then B chunks, dealt round-robin over all threads, so that
-    // no thread decodes more than ceil((A + B) / NT) chunks.  Chunk h of a box row
+    // A chunks first, then B chunks, dealt round-robin over the decoder threads, so
+    // that none decodes more than ceil((A + B) / NDEC) chunks.  Chunk h of a box row
     // sits at 16-byte position h, or with SWZ at h XOR bits 7.. of the row's address.
     constexpr int HM = BK / 16 - 1;
     const uint32_t raw_u32 = smem_u32(raw);
@@ -418,9 +425,12 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       const int hs = TS::SWZ ? (h ^ (int)(((raw_u32 + (uint32_t)off_row) >> 7) & (uint32_t)HM)) : h;
       return *reinterpret_cast<const uint4*>(raw + off_row + hs * 16);
     };
+    const int warp = tid / 32;
+    const bool decoder = NDEC == NT || warp % 4 >= XW;
+    const int dt = NDEC == NT ? tid : ((warp / 4) * (4 - XW) + warp % 4 - XW) * 32 + tid % 32;
 #pragma unroll
     for (int r = 0; r < AB_PER; ++r) {
-      const int c = tid + r * NT;
+      const int c = decoder ? dt + r * NDEC : A_CHUNKS + B_CHUNKS;
       if (c < A_CHUNKS) {
         const int row = TS::SWZ ? c % BM : c / (BK / 16);
         const int h = TS::SWZ ? c / BM : c % (BK / 16);

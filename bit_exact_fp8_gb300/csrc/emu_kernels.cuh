@@ -543,8 +543,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     for (int i = 0; i < TM; ++i)
 #pragma unroll
       for (int j = 0; j < TN; ++j) {
-        const uint32_t m = __vmaxs2(E2[i][j], __byte_perm(E2[i][j], 0u, 0x1032));
-        const uint32_t e2 = __vmins2(__vmaxs2(m, c16_hi(cp[i][j])), kClampE2);
+        const uint32_t e2 = __vmins2(
+            __vimax3_s16x2(E2[i][j], __byte_perm(E2[i][j], 0u, 0x1032), c16_hi(cp[i][j])), kClampE2);
         sc[i][j] = kScaleBase - (e2 & 0x7F800000u);
         acc[i][j] = (G == 1 || gl == 0) ? fmul_rz(cp[i][j], __uint_as_float(sc[i][j])) : 0.0f;
       }

@@ -50,7 +50,8 @@ def test_linear_full():
 
 @pytest.mark.parametrize("cs", W.CONFIGS["square"], ids=lambda c: c.name)
 def test_square_ragged_full(cs):
-    # several 128 x 64 tiles with ragged tails in M, N and K (K % 128 = 16)
+    # several CTA tiles (64 x 32 for this slow shape) with ragged tails in M, N and K
+    # (K % 128 = 16)
     full_check(W.shrink(cs, 200, 144, 1040))
 
 

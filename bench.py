@@ -14,6 +14,11 @@ flush (a 256 MiB write, larger than the 129 MB L2) and bracketed by CUDA events 
 the launching stream; barrier + synchronize on both sides of the timed region; the
 maximum over ranks.  Clocks are sampled with nvidia-smi during the timed region.
 
+e2e: the same metric through the host-buffer call (scaled_mm_host): every step uploads
+its pinned host operands and copies its result back, inside the timed region; steps
+alternate between two streams and two staging buffers, so one step's upload runs under
+the previous step's GEMM.
+
 N > 1 (torchrun): every rank runs the same workload on its own GPU (the GEMM has no
 exchange step: replicas, weak scaling); value = all ranks' flops / max time.
 

@@ -408,7 +408,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     tma_load_2d(dst, &tmA, k, (int)m0, bar);
     tma_load_2d(dst + TS::RAW_A, &tmB, k, (int)n0, bar);
   };
-  // all threads: decode the raw slot of stage st into operand buffer buf
+  // the decoder threads: decode the raw slot of stage st into operand buffer buf
   auto decode_stage = [&](int64_t st, int buf) {
     const unsigned char* raw = smem + (int)(st % NS) * TS::RAW_STAGE;
     unsigned char* base = smem + TS::STAGE_OFF + buf * TS::STAGE_BYTES;

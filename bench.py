@@ -64,11 +64,17 @@ KERNEL_SOURCES = ("bit_exact_fp8_gb300/csrc/emu_kernels.cuh", "bit_exact_fp8_gb3
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: comments and blank space do not count, so a
+    comment edit keeps a profile summary valid and any code change invalidates it."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)     # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                   # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

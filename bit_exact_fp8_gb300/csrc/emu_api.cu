@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdlib>
@@ -81,17 +82,20 @@ constexpr bool is_deep_variant(int t) {
     if (kTiles[u].deep == t) return true;
   return false;
 }
-// SMs of the current device (152 on a GB300), cached per device
+// SMs of the current device (152 on a GB300), cached per device (atomics: the entry
+// points may be called from several host threads)
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  if (cached[dev] == 0) {
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
     int n = 0;
-    cached[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-                   n > 0) ? n : 152;
+    v = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            ? n : 152;
+    cached[dev].store(v, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return v;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda)
@@ -139,13 +143,14 @@ template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, int G, int
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
   auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK>;
-  // the dynamic shared memory limit is a per-function, per-device attribute
-  static bool configured[64] = {false};
+  // the dynamic shared memory limit is a per-function, per-device attribute; setting
+  // it twice (two host threads racing on the first call) is harmless
+  static std::atomic<bool> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TS::SMEM_BYTES);
-    if (dev >= 0 && dev < 64) configured[dev] = true;
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
   }
   CUtensorMap tmA, tmB;
   int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK, TS::SWZ);
@@ -175,14 +180,13 @@ int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
 // larger of the issue time of the CTAs an SM receives and the latency-bound time of
 // its waves of resident CTAs.  EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
 int choose_tile(const emu::GemmParams& p, bool slow) {
-  static int forced = -2;
-  if (forced == -2) {
-    forced = -1;
+  static const int forced = [] {         // read once (thread-safe static initialisation)
     const char* env = getenv("EMU_FP8_TILE");
     if (env)
       for (int t = 0; t < kNumTiles; ++t)
-        if (std::strcmp(env, kTiles[t].name) == 0) forced = t;
-  }
+        if (std::strcmp(env, kTiles[t].name) == 0) return t;
+    return -1;
+  }();
   auto usable = [&](int t) { return p.S == 1 || p.ktile % kTiles[t].bk == 0; };
   if (forced >= 0 && usable(forced)) return forced;
   auto ctas_of = [&](const TileInfo& ti) {

@@ -1,6 +1,7 @@
 """Several host threads call the library at once, each on its own CUDA stream:
 the device entry point (scaled_mm) and the host-buffer one (scaled_mm_host, whose
-enqueue is serialised by the library), with first-use initialisation racing too.
+enqueue is serialised by the library; its first use, which creates the library's
+stream pool, happens inside the threads).
 ctypes releases the GIL during the C calls, so the calls overlap.  Every result
 must equal the single-threaded one bit for bit."""
 import threading

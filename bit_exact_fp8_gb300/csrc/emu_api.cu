@@ -497,47 +497,63 @@ int emu_scaled_mm_host(const uint8_t* A_host, emu_fp8_t fmt_a, const uint8_t* B_
   if (rc != EMU_OK) return rc;
   cudaGetLastError();   // clear a stale launch error of an earlier call
   EMU_CK(cudaEventRecord(hp->entry, user));
-  EMU_CK(cudaStreamWaitEvent(hp->up, hp->entry, 0));
-  EMU_CK(cudaStreamWaitEvent(hp->down, hp->entry, 0));
-  for (int i = 0; i < kHostComputeStreams; ++i) EMU_CK(cudaStreamWaitEvent(hp->comp[i], hp->entry, 0));
-  // upload: scalars, A, then B slab by slab
-  emu::emu_set_scalars_kernel<<<1, 32, 0, hp->up>>>(scal, scale_a, scale_b,
-                                                      scale_result ? *scale_result : 1.0f);
-  EMU_CK(cudaGetLastError());
-  if (K > 0) EMU_CK(cudaMemcpyAsync(base + lay.a, A_host, (size_t)M * (size_t)K,
-                                    cudaMemcpyHostToDevice, hp->up));
-  for (int c = 0; c < nch; ++c) {
-    const int64_t n0 = slab(c), n1 = slab(c + 1);
-    if (K > 0)
-      EMU_CK(cudaMemcpyAsync(dB + (size_t)n0 * (size_t)K, B_host + (size_t)n0 * (size_t)K,
-                             (size_t)(n1 - n0) * (size_t)K, cudaMemcpyHostToDevice, hp->up));
-    EMU_CK(cudaEventRecord(hp->uploaded[c], hp->up));
+  auto enqueue_all = [&]() -> int {
+    EMU_CK(cudaStreamWaitEvent(hp->up, hp->entry, 0));
+    EMU_CK(cudaStreamWaitEvent(hp->down, hp->entry, 0));
+    for (int i = 0; i < kHostComputeStreams; ++i)
+      EMU_CK(cudaStreamWaitEvent(hp->comp[i], hp->entry, 0));
+    // upload: scalars, A, then B slab by slab
+    emu::emu_set_scalars_kernel<<<1, 32, 0, hp->up>>>(scal, scale_a, scale_b,
+                                                        scale_result ? *scale_result : 1.0f);
+    EMU_CK(cudaGetLastError());
+    if (K > 0) EMU_CK(cudaMemcpyAsync(base + lay.a, A_host, (size_t)M * (size_t)K,
+                                      cudaMemcpyHostToDevice, hp->up));
+    for (int c = 0; c < nch; ++c) {
+      const int64_t n0 = slab(c), n1 = slab(c + 1);
+      if (K > 0)
+        EMU_CK(cudaMemcpyAsync(dB + (size_t)n0 * (size_t)K, B_host + (size_t)n0 * (size_t)K,
+                               (size_t)(n1 - n0) * (size_t)K, cudaMemcpyHostToDevice, hp->up));
+      EMU_CK(cudaEventRecord(hp->uploaded[c], hp->up));
+    }
+    // compute: slab c on compute stream c mod 4, once its B slab has landed
+    for (int c = 0; c < nch; ++c) {
+      const int64_t n0 = slab(c), n1 = slab(c + 1);
+      cudaStream_t cs = hp->comp[c % kHostComputeStreams];
+      EMU_CK(cudaStreamWaitEvent(cs, hp->uploaded[c], 0));
+      const emu::GemmParams p = make_params(
+          dA, fmt_a, dB + (size_t)n0 * (size_t)K, fmt_b, M, n1 - n0, K, scal, scal + 1,
+          scale_result ? scal + 2 : nullptr, dOut + (size_t)M * (size_t)n0 * esz, out_dtype,
+          split_S, preset, split_S > 1 ? dPart + (size_t)split_S * (size_t)M * (size_t)n0 : nullptr);
+      const int r = enqueue(p, preset, fast_accum, cs);
+      if (r != EMU_OK) return r;
+      EMU_CK(cudaEventRecord(hp->computed[c], cs));
+    }
+    // download: each finished slab into its columns of out_host
+    for (int c = 0; c < nch; ++c) {
+      const int64_t n0 = slab(c), n1 = slab(c + 1);
+      EMU_CK(cudaStreamWaitEvent(hp->down, hp->computed[c], 0));
+      EMU_CK(cudaMemcpy2DAsync(static_cast<unsigned char*>(out_host) + (size_t)n0 * esz,
+                               (size_t)N * esz, dOut + (size_t)M * (size_t)n0 * esz,
+                               (size_t)(n1 - n0) * esz, (size_t)(n1 - n0) * esz, (size_t)M,
+                               cudaMemcpyDeviceToHost, hp->down));
+    }
+    EMU_CK(cudaEventRecord(hp->done, hp->down));
+    EMU_CK(cudaStreamWaitEvent(user, hp->done, 0));
+    return EMU_OK;
+  };
+  rc = enqueue_all();
+  if (rc != EMU_OK) {
+    // whatever was enqueued before the failure may still use the staging buffer and
+    // the host buffers: order the caller's stream after all of the pool's streams
+    // (best effort; the first error stays the one reported)
+    const std::string err = g_last_error;
+    cudaStream_t pool[2 + kHostComputeStreams] = {hp->up, hp->down};
+    for (int i = 0; i < kHostComputeStreams; ++i) pool[2 + i] = hp->comp[i];
+    for (cudaStream_t s : pool)
+      if (cudaEventRecord(hp->done, s) == cudaSuccess) cudaStreamWaitEvent(user, hp->done, 0);
+    g_last_error = err;
   }
-  // compute: slab c on compute stream c mod 4, once its B slab has landed
-  for (int c = 0; c < nch; ++c) {
-    const int64_t n0 = slab(c), n1 = slab(c + 1);
-    cudaStream_t cs = hp->comp[c % kHostComputeStreams];
-    EMU_CK(cudaStreamWaitEvent(cs, hp->uploaded[c], 0));
-    const emu::GemmParams p = make_params(
-        dA, fmt_a, dB + (size_t)n0 * (size_t)K, fmt_b, M, n1 - n0, K, scal, scal + 1,
-        scale_result ? scal + 2 : nullptr, dOut + (size_t)M * (size_t)n0 * esz, out_dtype, split_S,
-        preset, split_S > 1 ? dPart + (size_t)split_S * (size_t)M * (size_t)n0 : nullptr);
-    rc = enqueue(p, preset, fast_accum, cs);
-    if (rc != EMU_OK) return rc;
-    EMU_CK(cudaEventRecord(hp->computed[c], cs));
-  }
-  // download: each finished slab into its columns of out_host
-  for (int c = 0; c < nch; ++c) {
-    const int64_t n0 = slab(c), n1 = slab(c + 1);
-    EMU_CK(cudaStreamWaitEvent(hp->down, hp->computed[c], 0));
-    EMU_CK(cudaMemcpy2DAsync(static_cast<unsigned char*>(out_host) + (size_t)n0 * esz,
-                             (size_t)N * esz, dOut + (size_t)M * (size_t)n0 * esz,
-                             (size_t)(n1 - n0) * esz, (size_t)(n1 - n0) * esz, (size_t)M,
-                             cudaMemcpyDeviceToHost, hp->down));
-  }
-  EMU_CK(cudaEventRecord(hp->done, hp->down));
-  EMU_CK(cudaStreamWaitEvent(user, hp->done, 0));
-  return EMU_OK;
+  return rc;
 }
 
 int emu_scaled_mm_ex(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, emu_fp8_t fmt_b,

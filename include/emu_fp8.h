@@ -213,8 +213,10 @@ int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a,
  * call's uploads with another's GEMM.  The
  * call keeps no pointer after the stream completes.  Status codes and argument
  * checks are those of emu_scaled_mm_ex; EMU_EINVAL also for a short or misaligned
- * staging buffer; EMU_ECUDA when a copy or a stream operation fails.  Calls from
- * several host threads are serialised while they enqueue.
+ * staging buffer; EMU_ECUDA when a copy or a stream operation fails.  When a step
+ * fails after others were enqueued, the caller's stream is still ordered after
+ * them, so the buffers may be released once it completes (out_host then holds no
+ * valid result).  Calls from several host threads are serialised while they enqueue.
  */
 size_t emu_host_staging_bytes(int64_t M, int64_t N, int64_t K, int32_t split_S,
                               emu_out_t out_dtype);

@@ -109,6 +109,9 @@ size_t emu_workspace_bytes(int64_t M, int64_t N, int32_t split_S);
  * E5M2 x E5M2 is rejected (EMU_EREJECT).  E5M2 Inf codes follow IEEE on the
  * products (Inf*0 -> NaN, +Inf and -Inf -> NaN, otherwise +-Inf).
  * Results do not depend on the previous contents of out or of the workspace.
+ * The call may be captured in a CUDA graph (stream capture): its launches, with
+ * the operand tensor maps encoded at capture, replay on whatever the same buffers
+ * hold then, so the buffers must stay where they were at capture.
  */
 int emu_scaled_mm(const uint8_t* A, emu_fp8_t fmt_a,
                   const uint8_t* B, emu_fp8_t fmt_b,

@@ -157,9 +157,16 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   if (rc != EMU_OK) return rc;
   rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK, TS::SWZ);
   if (rc != EMU_OK) return rc;
-  dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)((p.M + TS::BM - 1) / TS::BM),
-            (unsigned)p.S);
-  kern<<<grid, TS::NT, TS::SMEM_BYTES, st>>>(p, tmA, tmB);
+  // row tiles go on grid.y, which holds at most 65535: taller problems take several
+  // launches, each starting at row tile m_tile0
+  const int64_t tiles_m = (p.M + TS::BM - 1) / TS::BM;
+  for (int64_t y0 = 0; y0 < tiles_m; y0 += 65535) {
+    emu::GemmParams q = p;
+    q.m_tile0 = y0;
+    const int64_t ny = tiles_m - y0 < 65535 ? tiles_m - y0 : 65535;
+    dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)ny, (unsigned)p.S);
+    kern<<<grid, TS::NT, TS::SMEM_BYTES, st>>>(q, tmA, tmB);
+  }
   return EMU_OK;
 }
 
@@ -382,6 +389,7 @@ emu::GemmParams make_params(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B,
   p.partial = static_cast<float*>(workspace);
   p.S = split_S; p.scheme = preset->split_scheme; p.ktile = preset->ktile;
   p.restart_blocks = preset->restart / preset->block_width;
+  p.m_tile0 = 0;
   return p;
 }
 

@@ -80,6 +80,7 @@ struct GemmParams {
   int scheme;              // 0 contiguous tiles, 1 round-robin tiles
   int ktile;               // k-tile width of the split rule
   int restart_blocks;      // slow accumulation: blocks per chunk (R / B)
+  int64_t m_tile0;         // row tile of blockIdx.y == 0 (a launch covers at most 65535)
 };
 
 // ---------------------------------------------------------------------------
@@ -356,7 +357,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int tid = threadIdx.x;
   const int gl = tid % G;                    // lane within the group
   const int ty = (tid / G) / WN, tx = (tid / G) % WN;
-  const int64_t m0 = (int64_t)blockIdx.y * BM;
+  const int64_t m0 = ((int64_t)blockIdx.y + p.m_tile0) * BM;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int s = blockIdx.z;
 

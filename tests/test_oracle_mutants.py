@@ -56,6 +56,21 @@ MUTANTS = [
     ("bf16 rounded toward zero",
      "return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 8, -126, 127, 8, MODE_RNE);",
      "return (uint16_t)round_to_format(v.neg, v.mag, v.exp2, 8, -126, 127, 8, MODE_RZ);"),
+    ("fp8 output: Inf saturates to NaN",
+     "  if (v.cls == 1) return sign | max_code;",
+     "  if (v.cls == 1) return 0x7F;"),
+    ("fp8 output truncated instead of rounded to nearest even",
+     "    if (shift <= 128 && (rem > half || (rem == half && (q & 1)))) q += 1;",
+     "    if (0) q += 1;"),
+    ("fp8 output: scale_result folded into alpha",
+     "    uint32_t z = has_sr ? f32_mul_rn(y, sr) : y;",
+     "    uint32_t z = has_sr ? f32_fma_plus0(acc, f32_mul_rn(alpha, sr)) : y;"),
+    ("fp8 output: overflow to NaN instead of the maximum",
+     "  if (cmp) return sign | max_code;",
+     "  if (cmp) return 0x7F;"),
+    ("fp8 output: E5M2 maximum taken as the Inf code",
+     "  const uint8_t max_code = fmt == FMT_E4M3FN ? 0x7E : 0x7B;",
+     "  const uint8_t max_code = fmt == FMT_E4M3FN ? 0x7E : 0x7C;"),
 ]
 
 

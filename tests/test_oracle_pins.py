@@ -632,6 +632,28 @@ def test_fp8_output_epilogue_rounds_scale_result_separately(orc):
             want = torch.from_numpy(z.copy()).clamp(-mx, mx).to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
             want = np.where(np.isnan(z), np.uint8(0x7F), want)
             assert np.array_equal(got, want), (sa, sb, sr, fmt)
+    # near FP8 rounding midpoints, where rounding y first and then multiplying by
+    # scale_result differs from one rounding of acc * RN(alpha * scale_result): the
+    # accumulators within 8 ulps of each midpoint / (alpha * sr)
+    for fmt in FMTS:
+        vals = torch.arange(256, dtype=torch.uint8).view(TORCH_FP8[fmt]).float().numpy()
+        vals = np.unique(vals[np.isfinite(vals) & (vals > 0)])
+        mids = (vals[:-1] + vals[1:]) / 2
+        mx = 448.0 if fmt == "e4m3fn" else 57344.0
+        for sa, sb, sr in ((0.7, 1.3, 3.0), (0.3, 0.9, 5.0), (1.1, 0.37, 0.3)):
+            alpha = np.float32(np.float32(sa) * np.float32(sb))
+            base = (mids / (np.float64(alpha) * np.float64(np.float32(sr)))).astype(np.float32)
+            near = (base.view(np.int32)[:, None] + np.arange(-8, 9, dtype=np.int32)[None, :])
+            accm = np.concatenate([near.ravel(), (near.ravel() | np.int32(-2**31))]).view(np.float32)
+            y = (accm.astype(np.float64) * np.float64(alpha)).astype(np.float32)
+            z = (y.astype(np.float64) * np.float64(np.float32(sr))).astype(np.float32)
+            want = torch.from_numpy(z.copy()).clamp(-mx, mx).to(TORCH_FP8[fmt]).view(torch.uint8).numpy()
+            one = (accm.astype(np.float64) *
+                   np.float64(np.float32(np.float64(alpha) * np.float64(np.float32(sr))))).astype(np.float32)
+            assert (torch.from_numpy(one.copy()).clamp(-mx, mx).to(TORCH_FP8[fmt]).view(torch.uint8)
+                    .numpy() != want).sum() > 0     # the cases do separate the two readings
+            got = orc.epilogue(bits32(accm), sa, sb, fmt, scale_result=sr)
+            assert np.array_equal(got, want), (sa, sb, sr, fmt)
     # without scale_result: the fp32 y converts directly
     got = orc.epilogue(bits32(acc), 1.0, 1.0, "e4m3fn")
     want = torch.from_numpy(acc.copy()).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()

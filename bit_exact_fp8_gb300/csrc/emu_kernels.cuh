@@ -507,8 +507,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
       for (int j = 0; j < TN; ++j) E2[i][j] = 0x80008000u;
   };
-  // one DPX add-max per output for this lane's k-pair q of the block at (lbase, k0)
-  auto pass1_pair = [&](const unsigned char* lbase, int k0, int q) {
+  // one DPX add-max per output for this lane's k-pair q of the block at (lbase, k0),
+  // into the maxima `E` (E2, or the next block's En)
+  auto pass1_pair_into = [&](uint32_t (&E)[TM][TN], const unsigned char* lbase, int k0, int q) {
     const uint32_t* sAl = reinterpret_cast<const uint32_t*>(lbase + TS::A_LAB);   // label pairs
     const uint32_t* sBl = reinterpret_cast<const uint32_t*>(lbase + TS::B_LAB);
     const int kp = k0 / 2 + q * G + gl;
@@ -518,15 +519,23 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-      for (int j = 0; j < TN; ++j) E2[i][j] = __viaddmax_s16x2(la[i], lb[j], E2[i][j]);
+      for (int j = 0; j < TN; ++j) E[i][j] = __viaddmax_s16x2(la[i], lb[j], E[i][j]);
   };
+  // Fast chains of the packed tiles with several blocks per stage take the next
+  // block's pass 1 (DPX, integer pipe) inside this block's pass-2 loop (FP32 pipe),
+  // so one instruction stream feeds both pipes; the stage's first block runs its
+  // own pass 1.
+  constexpr bool kFuse = PK && G == 1 && !SLOW && NBLK >= 2;
+  uint32_t En[TM][TN];   // the next block's maxima while fused
   // one block of every chain, from the decoded buffer at `base`
-  auto block_step = [&](const unsigned char* base, int k0) {
+  auto block_step = [&](const unsigned char* base, int k0, bool have_e2, bool fuse_next) {
     const float* sAv = reinterpret_cast<const float*>(base + TS::A_VAL);
     const float* sBv = reinterpret_cast<const float*>(base + TS::B_VAL);
-    pass1_reset();
+    if (!have_e2) {
+      pass1_reset();
 #pragma unroll
-    for (int q = 0; q < BLK / (2 * G); ++q) pass1_pair(base, k0, q);
+      for (int q = 0; q < BLK / (2 * G); ++q) pass1_pair_into(E2, base, k0, q);
+    }
     if (G > 1) {                          // the group's partial maxima
 #pragma unroll
       for (int off = 1; off < G; off <<= 1)
@@ -563,8 +572,15 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         }
       const f32x2_t* pAv = reinterpret_cast<const f32x2_t*>(sAv);
       const f32x2_t* pBv = reinterpret_cast<const f32x2_t*>(sBv);
+      if (kFuse && fuse_next) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) En[i][j] = 0x80008000u;
+      }
 #pragma unroll
       for (int q = 0; q < BLK / (2 * G); ++q) {
+        if (kFuse && fuse_next) pass1_pair_into(En, base, k0 + BLK, q);
         const int kp = k0 / 2 + q * G + gl;
         f32x2_t a2[TM], b2[TN];
         if (TM % 2 == 0) {
@@ -641,6 +657,12 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         blocks_in_chunk = 0;
       }
     }
+    if (kFuse && fuse_next) {
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j) E2[i][j] = En[i][j];
+    }
   };
 
   // decode stage st + 1 into the other buffer while nobody reads it, then one
@@ -660,7 +682,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     // slow chains: the blocks of a stage stay a loop (a restart may fall after any
     // of them; unrolled, the 64 x 40 tile's 32-product variant spilled registers)
 #pragma unroll (SLOW ? 1 : NBLK)
-    for (int bb = 0; bb < NBLK; ++bb) block_step(cur, bb * BLK);
+    for (int bb = 0; bb < NBLK; ++bb) block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK);
     if (st + 1 < n_stages) {
       timed_out = !full_wait(st + 1);
       decode_stage(st + 1, (int)((st + 1) & 1));

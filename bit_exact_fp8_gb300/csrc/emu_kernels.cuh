@@ -300,12 +300,17 @@ struct TileShape {
   static constexpr int NS = RAW_STAGE <= 1024 ? 8 : (BM >= 128 ? 3 : 4);   // ring depth
   // one decoded stage buffer: A values [BK][BM] f32 (packed pass 2: [BK/2][BM][2]),
   // A labels [BK/2][BM][2] i16, B values [BK][BN] f32 (or [BK/2][BN][2]), B labels
-  // [BK/2][BN][2] i16: labels of k-adjacent codes share one 32-bit word
+  // [BK/2][BN][2] i16: labels of k-adjacent codes share one 32-bit word.  The
+  // lane-split tiles (BM of 4, BN of 8 or 16, unswizzled) append PAD words to every 16
+  // codes' rows of values and every 8 k-pairs' rows of labels: a decoder warp writes
+  // eight 16-code chunks of each row at once, and without the pad all eight fall in
+  // one bank
+  static constexpr int PAD = G > 1 ? 4 : 0;
   static constexpr int A_VAL = 0;
-  static constexpr int A_LAB = A_VAL + BK * BM * 4;
-  static constexpr int B_VAL = A_LAB + BK * BM * 2;
-  static constexpr int B_LAB = B_VAL + BK * BN * 4;
-  static constexpr int STAGE_BYTES = ((B_LAB + BK * BN * 2) + 127) / 128 * 128;
+  static constexpr int A_LAB = A_VAL + (BK * BM + (BK / 16) * PAD) * 4;
+  static constexpr int B_VAL = A_LAB + (BK / 2 * BM + (BK / 16) * PAD) * 4;
+  static constexpr int B_LAB = B_VAL + (BK * BN + (BK / 16) * PAD) * 4;
+  static constexpr int STAGE_BYTES = ((B_LAB + (BK / 2 * BN + (BK / 16) * PAD) * 4) + 127) / 128 * 128;
   static constexpr int STAGE_OFF = NS * RAW_STAGE;
   static constexpr int LUT_BYTES = 2 * 256 * 8;
   static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
@@ -344,6 +349,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // across the warp's threads (the identity for TN = 2)
   auto b_slot = [](int n) { return ((n % TN) / 2) * (2 * WN) + (n / TN) * 2 + (n % 2); };
   constexpr int NS = TS::NS;
+  constexpr int PAD = TS::PAD;
+  static_assert(PAD == 0 || !PK, "the packed layouts are unpadded");
   static_assert(TN % 2 == 0, "labels are paired along N");
 
   extern __shared__ __align__(128) unsigned char smem_dyn[];
@@ -444,10 +451,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           if (PK) {
             *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = make_uint2(d0.x, d1.x);
           } else {
-            sAv[(h * 16 + j) * BM + row] = __uint_as_float(d0.x);
-            sAv[(h * 16 + j + 1) * BM + row] = __uint_as_float(d1.x);
+            sAv[(h * 16 + j) * BM + h * PAD + row] = __uint_as_float(d0.x);
+            sAv[(h * 16 + j + 1) * BM + h * PAD + row] = __uint_as_float(d1.x);
           }
-          sAl[(h * 8 + j / 2) * BM + row] = d0.y | (d1.y << 16);
+          sAl[(h * 8 + j / 2) * BM + h * PAD + row] = d0.y | (d1.y << 16);
         }
       } else if (c < A_CHUNKS + B_CHUNKS) {
         const int cb = c - A_CHUNKS;
@@ -463,10 +470,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
             *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
                 make_uint2(d0.x, d1.x);
           } else {
-            sBv[(h * 16 + j) * BN + col] = __uint_as_float(d0.x);
-            sBv[(h * 16 + j + 1) * BN + col] = __uint_as_float(d1.x);
+            sBv[(h * 16 + j) * BN + h * PAD + col] = __uint_as_float(d0.x);
+            sBv[(h * 16 + j + 1) * BN + h * PAD + col] = __uint_as_float(d1.x);
           }
-          sBl[(h * 8 + j / 2) * BN + col] = d0.y | (d1.y << 16);
+          sBl[(h * 8 + j / 2) * BN + h * PAD + col] = d0.y | (d1.y << 16);
         }
       }
     }
@@ -514,8 +521,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     const uint32_t* sBl = reinterpret_cast<const uint32_t*>(lbase + TS::B_LAB);
     const int kp = k0 / 2 + q * G + gl;
     uint32_t la[TM], lb[TN];
-    load_words(sAl + kp * BM + ty * TM, la);
-    load_words(sBl + kp * BN + tx * TN, lb);
+    load_words(sAl + kp * BM + (kp >> 3) * PAD + ty * TM, la);
+    load_words(sBl + kp * BN + (kp >> 3) * PAD + tx * TN, lb);
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -618,9 +625,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         const int kk = q * G + gl;
         float a[TM], b[TN];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ty * TM + i];
+        for (int i = 0; i < TM; ++i) a[i] = sAv[(k0 + kk) * BM + ((k0 + kk) >> 4) * PAD + ty * TM + i];
 #pragma unroll
-        for (int j = 0; j < TN; ++j) b[j] = sBv[(k0 + kk) * BN + tx * TN + j];
+        for (int j = 0; j < TN; ++j) b[j] = sBv[(k0 + kk) * BN + ((k0 + kk) >> 4) * PAD + tx * TN + j];
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll

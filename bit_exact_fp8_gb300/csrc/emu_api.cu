@@ -46,9 +46,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 //   K8   1 x 2,  4 x  4 x 8 lanes, BK 64:  4 x  8, each block split over 8 lanes
 //   K4   1 x 2,  4 x  8 x 4 lanes, BK 64:  4 x 16, each block split over 4 lanes
 //   K8H, K4H: the same with BK 128, so a stage's barrier and wait are shared by four
-//        32-product blocks: faster when an SM holds one or two CTAs (latency bound),
-//        slower when it holds more, so the chooser only swaps them in for K8/K4 in the
-//        first case, and only where every split starts on a multiple of 128
+//        32-product blocks: candidates only when every split starts on a multiple of
+//        128 and all CTAs fit in one wave of resident CTAs (with fewer resident CTAs
+//        than K8/K4, a second wave costs more than the shared barriers save)
 //        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
 //        CTA tile must stay tiny for every SM to get work; one or two products per
 //        lane and block, so they keep scalar FP32)
@@ -62,26 +62,21 @@ struct TileInfo {
   double ipm;                   // effective thread instructions per MAC at full load
   double lat;                   // one CTA alone on an SM
   double slow_factor;           // slow accumulation's extra cost
-  int deep;                     // BK-128 variant for light SM loads, or -1
+  bool one_wave;                // a candidate only if its CTAs fit in one wave
 };
 // resident is also the kernel's __launch_bounds__ minimum, which holds ptxas to
 // 65536 / (resident * threads) registers
 constexpr TileInfo kTiles[] = {
-    {"M40", 4, 2, 64, 40, 320, 1, 1, 128, 1, 6.2, 131.0, 1.0, -1},
-    {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 6.0, 200.0, 1.0, -1},
-    {"S", 2, 2, 16, 16, 64, 6, 6, 64, 1, 12.5, 52.0, 1.0, -1},
-    {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 51.0, 35.0, 1.0, 6},
-    {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 38.0, 38.4, 1.0, 7},
-    {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, -1},
-    {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 51.0, 25.0, 1.0, -1},
-    {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 38.0, 29.0, 1.0, -1},
+    {"M40", 4, 2, 64, 40, 320, 1, 1, 128, 1, 6.2, 131.0, 1.0, false},
+    {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 6.0, 200.0, 1.0, false},
+    {"S", 2, 2, 16, 16, 64, 6, 6, 64, 1, 11.5, 49.0, 1.0, false},
+    {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 38.0, 36.0, 1.0, false},
+    {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 33.0, 33.0, 1.0, false},
+    {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, false},
+    {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 35.0, 18.0, 1.0, true},
+    {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 26.0, 21.0, 1.0, true},
 };
 constexpr int kNumTiles = 8;
-constexpr bool is_deep_variant(int t) {
-  for (int u = 0; u < kNumTiles; ++u)
-    if (kTiles[u].deep == t) return true;
-  return false;
-}
 // SMs of the current device (152 on a GB300), cached per device (atomics: the entry
 // points may be called from several host threads)
 int sm_count() {
@@ -203,17 +198,16 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
   int best = -1;
   double best_cost = 0.0;
   for (int t = 0; t < kNumTiles; ++t) {
-    if (is_deep_variant(t) || !usable(t)) continue;
+    if (!usable(t)) continue;
     const TileInfo& ti = kTiles[t];
     const int resident = slow ? ti.resident_slow : ti.resident;
     const double per_sm = std::ceil(ctas_of(ti) / sms);
+    if (ti.one_wave && per_sm > resident) continue;
     const double t_issue = per_sm * ti.bm * ti.bn * ti.ipm / 128.0;
     const double t_latency = std::ceil(per_sm / resident) * ti.lat;
     const double est = std::max(t_issue, t_latency) * (slow ? ti.slow_factor : 1.0);
     if (best < 0 || est < best_cost) { best = t; best_cost = est; }
   }
-  const int deep = kTiles[best].deep;
-  if (deep >= 0 && usable(deep) && ctas_of(kTiles[deep]) <= 2.0 * sms) return deep;
   return best;
 }
 

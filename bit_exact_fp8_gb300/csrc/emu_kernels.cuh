@@ -290,6 +290,9 @@ struct TileShape {
   // warp decodes 32 consecutive rows of one 16-code chunk, so that its shared stores
   // hit 32 distinct banks and its 16-byte raw reads 8 distinct bank quads
   static constexpr bool SWZ = BM >= 32 && BN >= 32 && (BK == 32 || BK == 64 || BK == 128);
+  // RM: a decoder warp takes consecutive rows of one 16-code chunk (with SWZ, or with
+  // rows of at least 16), so that its stores of one code position hit distinct banks
+  static constexpr bool RM = SWZ || (BM >= 16 && BN >= 16);
   // ring of raw FP8 boxes filled by TMA, first in shared memory: A [BM][BK] then
   // B [BN][BK] bytes per slot; with SWZ every box starts on a 1024-byte boundary
   // (the swizzle pattern's period), the ring's base included
@@ -440,8 +443,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     for (int r = 0; r < AB_PER; ++r) {
       const int c = decoder ? dt + r * NDEC : A_CHUNKS + B_CHUNKS;
       if (c < A_CHUNKS) {
-        const int row = TS::SWZ ? c % BM : c / (BK / 16);
-        const int h = TS::SWZ ? c / BM : c % (BK / 16);
+        const int row = TS::RM ? c % BM : c / (BK / 16);
+        const int h = TS::RM ? c / BM : c % (BK / 16);
         const uint4 q = chunk(row * BK, h);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -458,8 +461,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         }
       } else if (c < A_CHUNKS + B_CHUNKS) {
         const int cb = c - A_CHUNKS;
-        const int col = TS::SWZ ? cb % BN : cb / (BK / 16);
-        const int h = TS::SWZ ? cb / BN : cb % (BK / 16);
+        const int col = TS::RM ? cb % BN : cb / (BK / 16);
+        const int h = TS::RM ? cb / BN : cb % (BK / 16);
         const uint4 q = chunk(TS::RAW_A + col * BK, h);
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll

@@ -689,9 +689,10 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   }
   for (int64_t st = 0; st < n_stages; ++st) {
     const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
-    // slow chains: the blocks of a stage stay a loop (a restart may fall after any
-    // of them; unrolled, the 64 x 40 tile's 32-product variant spilled registers)
-#pragma unroll (SLOW ? 1 : NBLK)
+    // slow chains of the large tiles: the blocks of a stage stay a loop (a restart
+    // may fall after any of them; unrolled, the 64 x 40 tile's 32-product variant
+    // spilled registers); the small tiles unroll them
+#pragma unroll (SLOW && BM * BN > 1024 ? 1 : NBLK)
     for (int bb = 0; bb < NBLK; ++bb) block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK);
     if (st + 1 < n_stages) {
       timed_out = !full_wait(st + 1);

@@ -1,7 +1,7 @@
 """Every CTA tile shape of the GEMM kernel, forced one at a time through
 EMU_FP8_TILE (read once per process, hence one subprocess per tile), is bit-exact
 against the oracle on ragged shapes, both presets, fast and slow accumulation,
-split-K and the three output dtypes."""
+split-K, the three output dtypes, and Inf and NaN codes."""
 import os
 import subprocess
 import sys
@@ -28,6 +28,17 @@ cases = [
 for cs in cases:
     a, b = W.make_inputs(cs)
     assert_bits_equal(gpu_run(cs, a, b), oracle_full(cs, a, b), cs.name)
+# Inf and NaN codes: IEEE sums through every tile's block reduction
+for fast, S in ((True, 1), (False, 2)):
+    cs = W.Case("t6", 24, 32, 512, "e5m2", "e4m3fn", "f32", fast_accum=fast, split_S=S, seed=6)
+    a, b = W.make_inputs(cs)
+    a[2, 10] = 0x7C            # +Inf
+    a[5, 11] = 0xFC            # -Inf
+    a[5, 300] = 0x7C           # +Inf and -Inf in one row: NaN
+    b[:, 60] = 0x00
+    a[9, 60] = 0x7C            # Inf x 0: NaN
+    a[13, 200] = 0x7E          # NaN code
+    assert_bits_equal(gpu_run(cs, a, b), oracle_full(cs, a, b), f"t6 fast={fast} S={S}")
 print("ok")
 '''
 

@@ -382,11 +382,14 @@ def run_gpu(args, cs):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
+        config = config_dict(cs, "flushed between timed steps (256 MiB write)")
+        config["tile"] = api.tile_for(cs.M, cs.N, cs.K, use_fast_accum=cs.fast_accum,
+                                      splitk=cs.split_S, preset=cs.preset)
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic",
-                "config": config_dict(cs, "flushed between timed steps (256 MiB write)"),
+                "config": config,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "wall_s_timed_region": wall}

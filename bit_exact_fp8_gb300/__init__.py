@@ -10,8 +10,8 @@ The C ABI is include/emu_fp8.h (libemufp8.so, built by ``build.build()``);
 """
 from .api import (EmuCudaError, EmuError, ReferenceRejectsError, UnsupportedFeatureError,
                   accumulate, preset_params, scaled_mm, scaled_mm_host, staging_bytes,
-                  workspace_bytes)
+                  tile_for, workspace_bytes)
 
 __all__ = ["scaled_mm", "scaled_mm_host", "accumulate", "preset_params", "workspace_bytes",
-           "staging_bytes", "EmuError", "ReferenceRejectsError", "UnsupportedFeatureError",
+           "staging_bytes", "tile_for", "EmuError", "ReferenceRejectsError", "UnsupportedFeatureError",
            "EmuCudaError"]

@@ -27,7 +27,7 @@ EMU_OUT_E5M2 = 4
 EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
             "emu_abi_version", "emu_scaled_mm_noalloc", "emu_device_status",
             "emu_selftest_wait_timeout", "emu_scaled_mm_ex", "emu_host_staging_bytes",
-            "emu_scaled_mm_host")
+            "emu_scaled_mm_host", "emu_tile_for")
 
 #: size of the static scratch of emu_scaled_mm_noalloc (EMU_NOALLOC_SCRATCH_BYTES)
 EMU_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -87,6 +87,10 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.emu_device_status.restype = ctypes.c_int
     L.emu_selftest_wait_timeout.argtypes = [P]
     L.emu_selftest_wait_timeout.restype = ctypes.c_int
+    L.emu_tile_for.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                               ctypes.c_int32, ctypes.POINTER(emu_preset_t), ctypes.c_int32,
+                               ctypes.c_char_p, ctypes.c_size_t]
+    L.emu_tile_for.restype = ctypes.c_int
     L.emu_last_error.argtypes = []
     L.emu_last_error.restype = ctypes.c_char_p
     L.emu_abi_version.argtypes = []
@@ -169,6 +173,15 @@ def emu_device_status(reset: bool = False) -> int:
 
 def emu_selftest_wait_timeout(stream: int = 0) -> int:
     return int(load().emu_selftest_wait_timeout(ctypes.c_void_p(stream)))
+
+
+def emu_tile_for(M: int, N: int, K: int, fast_accum: int, split_S: int, preset: emu_preset_t,
+                 sm_count: int = 0) -> "tuple[int, str]":
+    """(status, tile name) of emu_tile_for."""
+    buf = ctypes.create_string_buffer(16)
+    st = load().emu_tile_for(M, N, K, int(fast_accum), int(split_S), ctypes.byref(preset),
+                             int(sm_count), buf, len(buf))
+    return int(st), buf.value.decode()
 
 
 def emu_scaled_mm_ex(A: int, fmt_a: int, B: int, fmt_b: int, M: int, N: int, K: int,

@@ -60,6 +60,17 @@ def workspace_bytes(M: int, N: int, split_S: int) -> int:
     return _lib.emu_workspace_bytes(M, N, split_S)
 
 
+def tile_for(M: int, N: int, K: int, *, use_fast_accum: bool = False, splitk: int = 1,
+             preset: Union[str, dict, "_lib.emu_preset_t"] = "hopper", sm_count: int = 0) -> str:
+    """Name of the CTA tile ``scaled_mm`` launches for an (M, N, K) problem ("none"
+    when nothing is launched); ``sm_count`` > 0 stands in for the device's."""
+    st, name = _lib.emu_tile_for(M, N, K, int(use_fast_accum), splitk, preset_params(preset),
+                                 sm_count)
+    if st != _lib.EMU_OK:
+        _raise(st, "tile_for")
+    return name
+
+
 def scaled_mm(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
               scale_b: torch.Tensor, bias: Optional[torch.Tensor] = None,
               scale_result: Optional[torch.Tensor] = None,

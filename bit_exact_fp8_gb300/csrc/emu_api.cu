@@ -181,7 +181,7 @@ int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
 // Pick the tile with the lowest estimated time per K element, in SM clocks: the
 // larger of the issue time of the CTAs an SM receives and the latency-bound time of
 // its waves of resident CTAs.  EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
-int choose_tile(const emu::GemmParams& p, bool slow) {
+int choose_tile(const emu::GemmParams& p, bool slow, double sms) {
   static const int forced = [] {         // read once (thread-safe static initialisation)
     const char* env = getenv("EMU_FP8_TILE");
     if (env)
@@ -194,7 +194,6 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
   auto ctas_of = [&](const TileInfo& ti) {
     return (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
   };
-  const double sms = sm_count();
   int best = -1;
   double best_cost = 0.0;
   for (int t = 0; t < kNumTiles; ++t) {
@@ -212,7 +211,7 @@ int choose_tile(const emu::GemmParams& p, bool slow) {
 }
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
-  switch (choose_tile(p, slow)) {
+  switch (choose_tile(p, slow, sm_count())) {
     case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1>(p, blk, slow, st);
     case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3>(p, blk, slow, st);
     case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6>(p, blk, slow, st);
@@ -619,6 +618,26 @@ int emu_device_status(int32_t* status, int32_t reset) {
     if (e != cudaSuccess) return fail(EMU_ECUDA, "clearing the device status failed: %s",
                                       cudaGetErrorString(e));
   }
+  return EMU_OK;
+}
+
+int emu_tile_for(int64_t M, int64_t N, int64_t K, int32_t fast_accum, int32_t split_S,
+                 const emu_preset_t* preset, int32_t sms, char* name, size_t name_len) {
+  g_last_error.clear();
+  if (!name || name_len == 0) return fail(EMU_EINVAL, "name buffer is null or empty");
+  name[0] = '\0';
+  const int rc = check_args(EMU_E4M3FN, EMU_E4M3FN, M, N, K, false, EMU_OUT_F32, split_S, preset);
+  if (rc != EMU_OK) return rc;
+  if (sms < 0) return fail(EMU_EINVAL, "sm_count %d is negative", sms);
+  const char* t = "none";                // nothing launches a GEMM tile
+  if (M > 0 && N > 0 && K > 0) {
+    const emu::GemmParams p = make_params(nullptr, EMU_E4M3FN, nullptr, EMU_E4M3FN, M, N, K,
+                                          nullptr, nullptr, nullptr, nullptr, EMU_OUT_F32,
+                                          split_S, preset, nullptr);
+    t = kTiles[choose_tile(p, fast_accum == 0, sms > 0 ? (double)sms : (double)sm_count())].name;
+  }
+  if (std::strlen(t) + 1 > name_len) return fail(EMU_EINVAL, "name buffer of %zu bytes is too small", name_len);
+  std::strcpy(name, t);
   return EMU_OK;
 }
 

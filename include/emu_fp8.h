@@ -244,6 +244,22 @@ int emu_scaled_mm_host(const uint8_t* A_host, emu_fp8_t fmt_a,
 int emu_device_status(int32_t* status, int32_t reset);
 
 /*
+ * The CTA tile the GEMM entry points launch for this problem (the format pair and
+ * the output dtype do not enter the choice), by its name: "M40", "M32", "M64",
+ * "S", "K8", "K4", "K8H" or "K4H", or "none" when M, N or K is 0.  The choice is
+ * this library's cost model of the GB300 (an estimate per tile of issue and
+ * latency time, fitted to measurements), not a behaviour of the pages' platforms;
+ * every tile gives the same bits.  sm_count > 0 stands in for the device's SM
+ * count, so the call needs no device; 0 asks the current device (152 when none is
+ * visible).  EMU_FP8_TILE=<name> forces a tile, as for the GEMM calls.  name
+ * receives the NUL-terminated name (name_len bytes at most; 4 suffice).  Returns
+ * EMU_OK, or the status the GEMM entry points return for the same sizes, split and
+ * preset, or EMU_EINVAL for a null or short buffer or a negative sm_count.
+ */
+int emu_tile_for(int64_t M, int64_t N, int64_t K, int32_t fast_accum, int32_t split_S,
+                 const emu_preset_t* preset, int32_t sm_count, char* name, size_t name_len);
+
+/*
  * Self-test of the bounded wait: enqueues a one-CTA kernel whose barrier can never
  * complete, so its wait gives up after a short limit and sets the device status
  * to 1 (read it with emu_device_status).  It exercises the failure path without a

@@ -1,0 +1,95 @@
+"""The tile chooser (host logic, no device): for the benchmark workloads and the
+small-M linear shapes, the tile emu_tile_for names is the fastest forced tile of
+the GB300 sweeps (median of 15 event-timed calls per tile, L2 flushed between
+calls), and EMU_FP8_TILE forces a tile where its K-stage fits the split.  Every
+tile gives the same bits (tests/test_gpu_tiles.py); these tests guard speed only."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152   # GB300
+
+# (M, N, K, fast, S, preset) -> the measured fastest tiles (a set where two tied)
+MEASURED_BEST = [
+    ((16, 64, 256, True, 1, "hopper"), {"K8H"}),              # the small case
+    ((64, 5760, 1920, True, 1, "hopper"), {"M40"}),           # linear layer
+    ((64, 5760, 1920, False, 1, "hopper"), {"M40"}),
+    ((4096, 4096, 4096, False, 1, "hopper"), {"M32"}),        # square, slow
+    ((8192, 5760, 1920, True, 1, "hopper"), {"M64"}),         # projections
+    ((8192, 1920, 1920, True, 1, "hopper"), {"M64"}),
+    ((16, 256, 262144, True, 2, "hopper"), {"K8H"}),          # split-K
+    ((16, 256, 262144, False, 2, "hopper"), {"K8H"}),
+    ((16, 256, 262144, True, 2, "ada"), {"K4"}),
+    ((16, 256, 262144, False, 2, "ada"), {"K4"}),
+    ((16, 256, 262144, True, 8, "hopper"), {"S"}),
+    ((16, 256, 262144, True, 8, "ada"), {"S"}),
+    ((16, 256, 262144, True, 24, "hopper"), {"S"}),
+    ((16, 256, 262144, False, 24, "ada"), {"S"}),
+    ((1, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),     # small M
+    ((2, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),
+    ((4, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),
+    ((8, 5760, 1920, True, 1, "hopper"), {"S", "K4H"}),
+    ((12, 1920, 1920, True, 1, "hopper"), {"K4H"}),
+    ((16, 5760, 1920, True, 1, "hopper"), {"S"}),
+    ((32, 5760, 1920, True, 1, "hopper"), {"S"}),
+]
+
+
+@pytest.mark.parametrize("shape,best", MEASURED_BEST, ids=lambda v: str(v))
+def test_pick_is_the_measured_fastest_tile(shape, best):
+    from bit_exact_fp8_gb300 import tile_for
+    M, N, K, fast, S, preset = shape
+    assert tile_for(M, N, K, use_fast_accum=fast, splitk=S, preset=preset, sm_count=SMS) in best
+
+
+def test_bk128_tiles_only_where_every_split_starts_on_a_multiple_of_128():
+    from bit_exact_fp8_gb300 import tile_for
+    # ada deals 64-wide k-tiles: a split may start at an odd multiple of 64
+    for S in (2, 3, 5, 8, 24):
+        for M, N in ((4, 64), (16, 256), (1, 5760)):
+            assert tile_for(M, N, 64 * 1024, use_fast_accum=True, splitk=S, preset="ada",
+                            sm_count=SMS) not in ("K8H", "K4H", "M40")
+
+
+def test_no_launch_and_rejections():
+    from bit_exact_fp8_gb300 import ReferenceRejectsError, tile_for
+    assert tile_for(0, 64, 256, sm_count=SMS) == "none"
+    assert tile_for(16, 0, 256, sm_count=SMS) == "none"
+    assert tile_for(16, 64, 0, sm_count=SMS) == "none"
+    with pytest.raises(ReferenceRejectsError):
+        tile_for(16, 72, 256, sm_count=SMS)          # N % 16 != 0
+    with pytest.raises(ValueError):
+        tile_for(16, 64, 256, splitk=0, sm_count=SMS)
+    with pytest.raises(ValueError):
+        tile_for(16, 64, 256, sm_count=-1)
+
+
+def test_the_sm_count_enters_the_choice():
+    from bit_exact_fp8_gb300 import tile_for
+    # with a quarter of the SMs the linear layer's 144 CTAs of 64 x 40 would take four
+    # waves, and a tile with two resident CTAs per SM is estimated faster
+    assert tile_for(64, 5760, 1920, use_fast_accum=True, sm_count=152) == "M40"
+    assert tile_for(64, 5760, 1920, use_fast_accum=True, sm_count=38) != "M40"
+
+
+CHILD = r'''
+import sys
+from bit_exact_fp8_gb300 import tile_for
+print(tile_for(16, 256, 262144, use_fast_accum=True, splitk=2, preset=sys.argv[1], sm_count=152))
+'''
+
+
+@pytest.mark.parametrize("forced,preset,want", [("K4", "hopper", "K4"), ("M64", "ada", "M64"),
+                                                ("K8H", "ada", "K4"), ("nonsense", "hopper", "K8H")])
+def test_forced_tile(forced, preset, want):
+    # EMU_FP8_TILE is read once per process; a BK-128 tile cannot take a split that
+    # starts off a multiple of 128 (ada), and an unknown name is ignored: the
+    # chooser's pick runs instead
+    env = dict(os.environ, EMU_FP8_TILE=forced)
+    r = subprocess.run([sys.executable, "-c", CHILD, preset], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == want

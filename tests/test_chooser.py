@@ -31,7 +31,7 @@ MEASURED_BEST = [
     ((1, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),     # small M
     ((2, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),
     ((4, 5760, 1920, True, 1, "hopper"), {"K4H", "K8H"}),
-    ((8, 5760, 1920, True, 1, "hopper"), {"S", "K4H"}),
+    ((8, 5760, 1920, True, 1, "hopper"), {"S"}),
     ((12, 1920, 1920, True, 1, "hopper"), {"K4H"}),
     ((16, 5760, 1920, True, 1, "hopper"), {"S"}),
     ((32, 5760, 1920, True, 1, "hopper"), {"S"}),

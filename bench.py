@@ -1,26 +1,45 @@
 """Benchmark of the emulated FP8 scaled GEMM on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--shard replicas|columns]
 
 One step = one emu_scaled_mm call over one batch of synthetic inputs already
 resident in HBM: decode, block-aligned truncating accumulation, split combine and
-epilogue (every step of the hot path).  The default workload is the linear-layer
-shape of the documentation's example (M=64, K=1920, N=5760, E4M3 x E4M3, bf16
-output, fast accumulation, S=1, hopper preset).  The metric is emulated TFLOP/s =
-2*M*N*K / time.
+epilogue (every step of the hot path).  The default workload is the projection
+batch, the largest single-GPU workload (M=8192 tokens, K=1920, N=5760, E4M3 x E4M3,
+bf16 output, fast accumulation, S=1, hopper preset).  The metric is emulated
+TFLOP/s = 2*M*N*K / time.
 
 Timing: W untimed warm-up steps; then K steps, each preceded by an untimed L2
 flush (a 256 MiB write, larger than the 129 MB L2) and bracketed by CUDA events on
 the launching stream; barrier + synchronize on both sides of the timed region; the
-maximum over ranks.  Clocks are sampled with nvidia-smi during the timed region.
+maximum over ranks.  SM clocks and throttle reasons are sampled through NVML every
+10 ms during the timed region (nvidia-smi every 200 ms when NVML cannot be loaded).
+
+Roofline: the denominators are measured in the same run by libemupeaks (the
+instruction rates of the pipes the kernel issues on, lane-operations per clock per
+SM) times the SM count and the maximum SM clock.  The headline fraction is against
+the rate at which the GB300 issues the kernel's own per-MAC arithmetic (1.5 packed
+f32x2 instructions and 0.5 DPX add-max); beside it the FP32 pipe alone, the
+algorithmic count of 5 integer lane-operations per MAC against the measured
+integer peak, and for the split-K shapes the HBM bytes against the measured HBM
+bandwidth and the serial-chain latency per block.
+
+CPU baseline and parity: the CPU oracle (exact integer arithmetic, every host
+thread) is timed on stripes of the same workload -- a 64-row stripe, then column
+slabs -- and every output it produces is compared bit for bit with the timed GPU
+output; the line carries "parity": {"checked", "mismatches"}, and the run fails
+on any mismatch.
 
 e2e: the same metric through the host-buffer call (scaled_mm_host): every step uploads
 its pinned host operands and copies its result back, inside the timed region; steps
 alternate between two streams and two staging buffers, so one step's upload runs under
 the previous step's GEMM.
 
-N > 1 (torchrun): every rank runs the same workload on its own GPU (the GEMM has no
-exchange step: replicas, weak scaling); value = all ranks' flops / max time.
+N > 1 (torchrun): --shard replicas (default): every rank runs the whole workload on
+its own GPU (the GEMM has no exchange step; weak scaling); --shard columns: the
+ranks split N into column slabs of the one workload (strong scaling, no data-path
+collective).  value = all ranks' flops / the maximum time over ranks.
 
 --impl reference runs the CPU oracle (the slow, exact reference model) on the host
 cores on a bounded sample of the same workload, rank 0 only.
@@ -28,11 +47,13 @@ cores on a bounded sample of the same workload, rank 0 only.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 import numpy as np
@@ -46,9 +67,8 @@ from bit_exact_fp8_gb300 import workloads as W  # noqa: E402
 
 METRIC = "emulated FP8 GEMM TFLOP/s (2MNK/s) bit-exact vs oracle; % of INT-ALU/HBM roofline"
 UNIT = "TFLOP/s"
-SMS = 152
-LANES_PER_SM = 128          # 4 sub-partitions x 32 lanes: one warp instruction per clock each
-OPS_PER_MAC = 5             # exponent add, max, significand multiply, align shift, add
+DEFAULT_WORKLOAD = "projection-N5760"
+OPS_PER_MAC = 5             # algorithmic: exponent add, max, significand multiply, align shift, add
 FP32_OPS_PER_MAC = 3        # the kernel's exact product, truncating multiply and exact add
 
 
@@ -78,30 +98,39 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary of
-    this workload, if it was taken on the current kernel sources (else None)."""
+def profile_summary(workload: str):
+    """The committed ncu summary of this workload's GEMM launch, if it was taken on
+    the current kernel sources: {"traffic": DRAM bytes per launch, "ncu": {...}}."""
     path = os.path.join(ROOT, "profiles", f"emu_gemm_{workload}.md")
     if not os.path.exists(path):
         return None
-    fields = {}
+    fields, table = {}, {}
     with open(path) as f:
         for line in f:
             if line.startswith("- ") and ":" in line:
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
+            elif line.startswith("| ") and line.count("|") == 3:
+                k, v = [x.strip() for x in line.strip().strip("|").split("|")]
+                table[k] = v
     if fields.get("kernel source sha256") != kernel_source_hash():
         return None
+
+    def num(key):
+        try:
+            return float(table[key].split()[0])
+        except (KeyError, ValueError, IndexError):
+            return None
     try:
-        return float(fields["dram bytes per launch"])
+        traffic = float(fields["dram bytes per launch"])
     except (KeyError, ValueError):
-        return None
-
-
-def alu_peak_tops(peaks):
-    """Issue-slot peak of 32-bit lane operations: SMs x 128 lanes x max SM clock."""
-    mhz = (peaks or {}).get("sm_max_mhz", 2070.0)
-    return SMS * LANES_PER_SM * mhz * 1e6 / 1e12, mhz
+        traffic = None
+    return {"traffic": traffic,
+            "ncu": {"source": os.path.relpath(path, ROOT),
+                    "issue_active_pct": num("smsp__issue_active.avg.pct_of_peak_sustained_active"),
+                    "fma_pipe_pct": num("sm__pipe_fma_cycles_active.avg.pct_of_peak_sustained_active"),
+                    "alu_pipe_pct": num("sm__pipe_alu_cycles_active.avg.pct_of_peak_sustained_active"),
+                    "shared_pipe_pct": num("l1tex__data_pipe_lsu_wavefronts_mem_shared.sum.pct_of_peak_sustained_elapsed")}}
 
 
 def dist_env():
@@ -111,30 +140,95 @@ def dist_env():
     return ws, rank, local
 
 
-class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
+
+class Clocks:
+    """SM clock, power and throttle reasons of one GPU, sampled every 10 ms through
+    NVML (libnvidia-ml, read-only queries) from a host thread; falls back to
+    nvidia-smi every 200 ms when NVML cannot be loaded."""
+
+    def __init__(self, dev: torch.device):
+        self.dev = dev
+        self.samples = []
+        self.nvml = None
+        self.handle = None
         self.proc = None
-        self.out = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+        self._stop = threading.Event()
+        try:
+            self._open_nvml()
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _open_nvml(self):
+        L = ctypes.CDLL("libnvidia-ml.so.1")
+        if L.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.dev)
+        ok = False
+        if all(hasattr(props, k) for k in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+            for fmt in ("{:08x}:{:02x}:{:02x}.0", "{:04x}:{:02x}:{:02x}.0"):
+                bus = fmt.format(props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+                if L.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0:
+                    ok = True
+                    break
+        if not ok and hasattr(props, "uuid"):
+            uid = ("GPU-" + str(props.uuid)).encode()
+            ok = L.nvmlDeviceGetHandleByUUID(uid, ctypes.byref(h)) == 0
+        if not ok:
+            raise OSError("no NVML handle for the CUDA device")
+        self.nvml, self.handle = L, h
+        self.reason_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(L, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+
+    def _poll(self):
+        L, h = self.nvml, self.handle
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if L.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                p = pw.value / 1e3 if L.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                r = rs.value if self.reason_fn(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), p, int(r)))
+            self._stop.wait(0.010)
 
     def start(self):
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
+            self.out = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
             self.f = open(self.out, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", str(self.dev.index or 0),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
+        except OSError:
             self.proc = None
 
     def stop(self):
+        if self.nvml is not None:
+            self._stop.set()
+            self.thread.join(timeout=5)
+            sm = [s[0] for s in self.samples]
+            reasons = sorted({name for _, _, r in self.samples for bit, name in _REASONS.items()
+                              if r & bit})
+            pw = [s[1] for s in self.samples if s[1] is not None]
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                    "samples": len(sm), "sampler": "nvml 10 ms",
+                    "power_w_max": max(pw) if pw else None, "reasons": reasons}
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": ["no clock sampler available"]}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -146,20 +240,20 @@ class Clocks:
         with open(self.out) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 7:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
                 except ValueError:
                     continue
-                for nm, v in zip(names, parts[5:9]):
+                for nm, v in zip(names, parts[3:7]):
                     if v.lower() == "active":
                         reasons.add(nm)
         os.unlink(self.out)
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+                "sampler": "nvidia-smi 200 ms", "reasons": sorted(reasons)}
 
 
 def torch_fp8(fmt):
@@ -168,6 +262,13 @@ def torch_fp8(fmt):
 
 def out_torch_dtype(od):
     return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[od]
+
+
+def out_bits(y: torch.Tensor) -> np.ndarray:
+    y = y.cpu()
+    if y.dtype == torch.float32:
+        return y.view(torch.int32).numpy().view(np.uint32)
+    return y.view(torch.int16).numpy().view(np.uint16)
 
 
 def config_dict(cs, l2_note):
@@ -179,31 +280,77 @@ def config_dict(cs, l2_note):
             "preset": cs.preset, "l2": l2_note}
 
 
+def dtype_label(cs):
+    return f"{cs.fmt_a}x{cs.fmt_b}->{cs.out_dtype}"
+
+
+def blocks_per_chain(cs):
+    """32- or 16-product blocks in one split's chain (the longest split)."""
+    B = 32 if cs.preset == "hopper" else 16
+    kt = 128 if cs.preset == "hopper" else 64
+    T = -(-cs.K // kt)
+    per_split = -(-T // cs.split_S) * kt
+    return -(-min(cs.K, per_split) // B)
+
+
 # ---------------------------------------------------------------------------
-def oracle_rate(cs, a, b, budget_s: float):
-    """Time the CPU oracle (as it stands) on column slices of the workload until
-    about budget_s seconds of work; returns (TFLOP/s, cores, sample description)."""
+def oracle_leg(cs, a, b, budget_s: float, got=None):
+    """The CPU oracle as it stands, on every host thread, timed on stripes of the
+    workload until about budget_s seconds of work: a 64-row stripe first (every
+    output of a workload with M <= 64), then column slabs at rotating offsets.
+    When ``got`` (the timed GPU output's bits) is given, every output the oracle
+    produces is compared with it.  Returns (TFLOP/s, cores, sample, parity)."""
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    ncols = 16
-    t_total, macs_total, reps = 0.0, 0, 0
-    start_col = 0
-    while t_total < budget_s:
-        cols = slice(start_col, start_col + ncols)
+    t_total, macs_total, checked, bad = 0.0, 0, 0, 0
+    first_bad = []
+    seen = np.zeros((cs.M, cs.N), dtype=bool) if got is not None else None
+
+    def run(a_part, b_part, rows, cols):
+        nonlocal t_total, macs_total, checked, bad
         t0 = time.perf_counter()
-        oracle.scaled_mm(a, b[cols], cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
-                         cs.fast_accum, cs.split_S, cs.preset, nthreads=cores)
+        want = oracle.scaled_mm(a_part, b_part, cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b,
+                                cs.out_dtype, cs.fast_accum, cs.split_S, cs.preset,
+                                nthreads=cores)
         dt = time.perf_counter() - t0
         t_total += dt
-        macs_total += a.shape[0] * ncols * a.shape[1]
-        reps += 1
-        start_col = (start_col + ncols) % max(1, b.shape[0] - ncols)
+        macs_total += a_part.shape[0] * b_part.shape[0] * a_part.shape[1]
+        if got is not None:
+            g = got[rows, cols]
+            diff = np.flatnonzero(g.ravel() != want.ravel())
+            checked += want.size
+            bad += diff.size
+            seen[rows, cols] = True
+            if diff.size and len(first_bad) < 5:
+                first_bad.append(f"rows {rows.start}.. cols {cols.start}..: {diff.size} differ")
+        return dt
+
+    rng = np.random.default_rng(2024)
+    r0 = int(rng.integers(0, max(1, cs.M - 64 + 1)))
+    rows = slice(r0, min(cs.M, r0 + 64))
+    run(a[rows], b, rows, slice(0, cs.N))
+    pieces = 1
+    ncols, c0 = 16, int(rng.integers(0, max(1, cs.N // 16))) * 16
+    while t_total < budget_s:
+        cols = slice(c0, min(cs.N, c0 + ncols))
+        dt = run(a, b[cols], slice(0, cs.M), cols)
+        pieces += 1
+        c0 = (c0 + 7 * 16 + ncols) % max(16, cs.N - ncols + 1) // 16 * 16
         if dt < budget_s / 20:
-            ncols = min(b.shape[0], ncols * 2)
-    sample = (f"{reps} oracle calls on column slices of the {cs.name} workload "
-              f"({macs_total / 1e9:.2f} GMAC, {t_total:.1f} s, all {cores} host threads)")
-    return 2.0 * macs_total / t_total / 1e12, cores, sample
+            ncols = min(cs.N, ncols * 2)
+    sample = (f"{pieces} oracle calls on stripes of the {cs.name} workload (a 64-row stripe, "
+              f"then column slabs; {macs_total / 1e9:.2f} GMAC, {t_total:.1f} s, all {cores} "
+              "host threads)")
+    parity = None
+    if got is not None:
+        parity = {"checked": int(checked), "mismatches": int(bad),
+                  "distinct_outputs": int(seen.sum()), "of_outputs": int(cs.M * cs.N),
+                  "what": "every output the CPU-baseline oracle calls produce, bit for bit "
+                          "against the timed GPU output"}
+        if first_bad:
+            parity["first"] = first_bad
+    return 2.0 * macs_total / t_total / 1e12, cores, sample, parity
 
 
 def run_reference(args, cs):
@@ -215,7 +362,7 @@ def run_reference(args, cs):
     import oracle
     oracle.build()
     cores = os.cpu_count() or 1
-    # bounded per-step sample: a column slice sized so the whole run takes ~60 s
+    # bounded per-step sample: a column slice sized so that the whole run takes ~60 s
     t0 = time.perf_counter()
     oracle.scaled_mm(a, b[:16], cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
                      cs.fast_accum, cs.split_S, cs.preset, nthreads=cores)
@@ -244,8 +391,62 @@ def run_reference(args, cs):
 
 
 # ---------------------------------------------------------------------------
+def roofline(cs, t_step, rates, peaks, sms, prof):
+    """The roofline object of the GEMM kernel (see the module docstring)."""
+    mhz = (peaks or {}).get("sm_max_mhz", 2070.0)
+    clk = sms * mhz * 1e6
+    macs = cs.M * cs.N * cs.K
+    tflops = 2.0 * macs / t_step / 1e12
+    mix = rates["emulation_mix_macs"]
+    packed = min(rates[k] for k in ("f32x2_fmul_rz_subnormal", "f32x2_fmul_rn_normal",
+                                    "f32x2_fadd_subnormal"))
+    int_peak = max(rates[k] for k in ("imad", "iadd3", "lop3", "prmt", "dpx_viaddmax_s16x2",
+                                      "imad_iadd3_mixed"))
+    peak = 2.0 * mix * clk / 1e12
+    roof = {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+            "frac": tflops / peak,
+            "traffic": prof["traffic"] if prof else None,
+            "note": (f"peak = measured issue rate of the kernel's per-MAC arithmetic (1.5 packed "
+                     f"f32x2 + 0.5 DPX per MAC: {mix:.1f} MAC/clk/SM, libemupeaks in this run) "
+                     f"x {sms} SMs x {mhz:.0f} MHz (sm_max_mhz); achieved = 2MNK / event time")}
+    roof["fp32_pipe"] = {"ops_per_mac": FP32_OPS_PER_MAC, "unit": "Tops/s",
+                         "achieved": FP32_OPS_PER_MAC * macs / t_step / 1e12,
+                         "peak": packed * clk / 1e12,
+                         "peak_lane_ops_per_clk_sm": packed,
+                         "frac": FP32_OPS_PER_MAC * macs / t_step / (packed * clk)}
+    roof["algorithmic"] = {"ops_per_mac": OPS_PER_MAC, "unit": "Tops/s",
+                           "achieved": OPS_PER_MAC * macs / t_step / 1e12,
+                           "peak": int_peak * clk / 1e12,
+                           "peak_lane_ops_per_clk_sm": int_peak,
+                           "frac": OPS_PER_MAC * macs / t_step / (int_peak * clk),
+                           "note": "5 integer lane-ops per MAC against the measured 32-bit integer "
+                                   "issue peak; the kernel does the work on the FP32 pipe, so "
+                                   "this fraction can exceed 1"}
+    roof["measured_issue_rates"] = {k: round(v, 2) for k, v in rates.items()}
+    if prof:
+        roof["ncu"] = prof["ncu"]
+    if peaks and "hbm_gbs" in peaks:
+        esz = 4 if cs.out_dtype == "f32" else 2
+        byts = cs.M * cs.K + cs.N * cs.K + cs.M * cs.N * esz
+        if cs.split_S > 1:
+            byts += 2 * cs.split_S * cs.M * cs.N * 4        # partials written and read back
+        roof["hbm"] = {"bytes_per_step": byts, "achieved_gbs": byts / t_step / 1e9,
+                       "peak_gbs": peaks["hbm_gbs"],
+                       "frac": byts / t_step / 1e9 / peaks["hbm_gbs"],
+                       "note": "algorithmic bytes (operands once, output, split partials) against "
+                               "the measured copy bandwidth of MEASURED_PEAKS.json"}
+    if cs.split_S > 1:
+        nb = blocks_per_chain(cs)
+        roof["latency"] = {"blocks_per_chain": nb,
+                           "sm_clocks_per_block": t_step * mhz * 1e6 / nb,
+                           "note": "serial blocks of one split's chain; clocks per block = step "
+                                   "time x max SM clock / blocks (combine kernel included)"}
+    return roof
+
+
 def run_gpu(args, cs):
-    from bit_exact_fp8_gb300 import _lib, api
+    from bit_exact_fp8_gb300 import _lib, api, peaks as peaks_mod
+    from bit_exact_fp8_gb300.sharding import column_slab
     ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
@@ -254,13 +455,17 @@ def run_gpu(args, cs):
     dev = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(dev)
     a, b = W.make_inputs(cs)
+    # column slabs: this rank's [n0, n1) of the one workload; replicas: all of it
+    n0, n1 = (column_slab(cs.N, rank, ws) if (ws > 1 and args.shard == "columns")
+              else (0, cs.N))
+    Nl = n1 - n0
     A = torch.from_numpy(a).to(dev).view(torch_fp8(cs.fmt_a))
-    Bt = torch.from_numpy(b).to(dev).view(torch_fp8(cs.fmt_b))
+    Bt = torch.from_numpy(np.ascontiguousarray(b[n0:n1])).to(dev).view(torch_fp8(cs.fmt_b))
     sa = torch.tensor(cs.scale_a, dtype=torch.float32, device=dev)
     sb = torch.tensor(cs.scale_b, dtype=torch.float32, device=dev)
     od = out_torch_dtype(cs.out_dtype)
-    out = torch.empty((cs.M, cs.N), dtype=od, device=dev)
-    need = api.workspace_bytes(cs.M, cs.N, cs.split_S)
+    out = torch.empty((cs.M, Nl), dtype=od, device=dev)
+    need = api.workspace_bytes(cs.M, Nl, cs.split_S)
     wsbuf = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     P = api.preset_params(cs.preset)
     stream = torch.cuda.current_stream(dev)
@@ -268,29 +473,33 @@ def run_gpu(args, cs):
     odc = {"f32": _lib.EMU_OUT_F32, "bf16": _lib.EMU_OUT_BF16, "f16": _lib.EMU_OUT_F16}
 
     def step():
+        if Nl == 0:
+            return
         st = _lib.emu_scaled_mm(A.data_ptr(), fmt[cs.fmt_a], Bt.data_ptr(), fmt[cs.fmt_b],
-                                cs.M, cs.N, cs.K, sa.data_ptr(), sb.data_ptr(), out.data_ptr(),
+                                cs.M, Nl, cs.K, sa.data_ptr(), sb.data_ptr(), out.data_ptr(),
                                 odc[cs.out_dtype], int(cs.fast_accum), cs.split_S, P,
                                 wsbuf.data_ptr(), wsbuf.numel(), stream.cuda_stream)
         if st != 0:
             raise RuntimeError(f"emu_scaled_mm failed: {st} {_lib.emu_last_error()}")
 
-    launches_per_step = 1 + (1 if cs.split_S > 1 else 0)
+    launches_per_step = (1 + (1 if cs.split_S > 1 else 0)) if Nl else 0
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize(dev)
+    # the roofline's denominators, measured on this GPU before the timed region
+    rates = peaks_mod.issue_rates()
+    torch.cuda.synchronize(dev)
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = Clocks(dev.index if ws == 1 else local)
+    clocks = Clocks(dev)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
-    time.sleep(0.3)                      # let the sampler take a first reading
     wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
@@ -299,39 +508,29 @@ def run_gpu(args, cs):
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    clk = clocks.stop()
     if ws > 1:
         dist.barrier()
-    clk = clocks.stop()
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     t_sum = sum(kernel_ms) / 1e3
     if ws > 1:
         from bit_exact_fp8_gb300.sharding import max_over_ranks
         t_sum = max_over_ranks(t_sum)
+    got = out_bits(out) if (rank == 0 and Nl == cs.N) else None
 
     flops_step = 2.0 * cs.M * cs.N * cs.K
-    value = ws * flops_step * args.steps / t_sum / 1e12
+    job_flops = flops_step * (ws if args.shard == "replicas" else 1)
+    value = job_flops * args.steps / t_sum / 1e12
     ms_step = 1e3 * t_sum / args.steps
 
     # roofline of the dominant kernel (the GEMM; for S > 1 the step also holds the
-    # small combine kernel, so the GEMM's share is taken from the profile summary)
-    peaks = measured_peaks()
-    peak, mhz = alu_peak_tops(peaks)
-    achieved = OPS_PER_MAC * cs.M * cs.N * cs.K / (t_sum / args.steps) / 1e12
-    traffic = args.traffic if args.traffic is not None else profiled_traffic(args.workload)
-    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s",
-            "frac": achieved / peak, "traffic": traffic,
-            "note": f"{OPS_PER_MAC} lane-ops per MAC (algorithmic); peak = {SMS} SMs x "
-                    f"{LANES_PER_SM} lanes x {mhz:.0f} MHz issue slots (recipe unit counts, "
-                    "sm_max_mhz of MEASURED_PEAKS.json)"}
-    # this implementation's own ceiling: pass 2 issues packed f32x2 instructions, so the
-    # FP32 pipe (128 operations per clock per SM) bounds it at 3 FP32 operations per MAC
-    roof["fp32_pipe"] = {"ops_per_mac": FP32_OPS_PER_MAC, "peak": peak,
-                         "achieved": FP32_OPS_PER_MAC * achieved / OPS_PER_MAC,
-                         "frac": FP32_OPS_PER_MAC * achieved / OPS_PER_MAC / peak}
-    if peaks and "hbm_gbs" in peaks:
-        bytes_step = cs.M * cs.K + cs.N * cs.K + cs.M * cs.N * (4 if cs.out_dtype == "f32" else 2)
-        roof["hbm_gbs"] = bytes_step / (t_sum / args.steps) / 1e9
-        roof["hbm_frac_of_measured"] = roof["hbm_gbs"] / peaks["hbm_gbs"]
+    # small combine kernel), on this rank's share of the work
+    mine = W.shrink(cs, cs.M, Nl, cs.K) if Nl != cs.N else cs
+    prof = profile_summary(args.workload) if (args.traffic is None and Nl == cs.N) else None
+    if args.traffic is not None:
+        prof = {"traffic": args.traffic, "ncu": {"source": "--traffic"}}
+    roof = roofline(mine, t_sum / args.steps, rates, measured_peaks(),
+                    torch.cuda.get_device_properties(dev).multi_processor_count, prof)
 
     # end to end through the public API's host-buffer call: every step uploads its
     # pinned host operands, computes and copies its result back into pinned host
@@ -340,14 +539,14 @@ def run_gpu(args, cs):
     # of calls, as a server would issue them); the region spans the first upload to
     # the last copy back.
     e2e = None
-    if rank == 0 or ws > 1:
+    if Nl and args.e2e_steps > 0:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         a_h = torch.from_numpy(a).view(torch_fp8(cs.fmt_a)).pin_memory()
-        b_h = torch.from_numpy(b).view(torch_fp8(cs.fmt_b)).pin_memory()
+        b_h = torch.from_numpy(np.ascontiguousarray(b[n0:n1])).view(torch_fp8(cs.fmt_b)).pin_memory()
         lanes = 2
         e2e_streams = [torch.cuda.Stream(dev) for _ in range(lanes)]
-        y_h = [torch.empty((cs.M, cs.N), dtype=od).pin_memory() for _ in range(lanes)]
-        stagings = [torch.empty(api.staging_bytes(cs.M, cs.N, cs.K, cs.split_S, od),
+        y_h = [torch.empty((cs.M, Nl), dtype=od).pin_memory() for _ in range(lanes)]
+        stagings = [torch.empty(api.staging_bytes(cs.M, Nl, cs.K, cs.split_S, od),
                                 dtype=torch.uint8, device=dev) for _ in range(lanes)]
 
         def e2e_call(i):
@@ -360,6 +559,8 @@ def run_gpu(args, cs):
         for i in range(2 * lanes):                       # warm-up (streams, pools, pages)
             e2e_call(i)
         torch.cuda.synchronize(dev)
+        if ws > 1:
+            dist.barrier()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(e2e_streams[0])
@@ -370,48 +571,60 @@ def run_gpu(args, cs):
         t1.record(e2e_streams[0])
         torch.cuda.synchronize(dev)
         t_e2e = t0.elapsed_time(t1) / 1e3
-        e2e = {"value": ws * flops_step * e2e_steps / t_e2e / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": a.nbytes + b.nbytes,
-               "d2h_bytes_per_step": cs.M * cs.N * y_h[0].element_size(), "steps": e2e_steps,
+        if ws > 1:
+            from bit_exact_fp8_gb300.sharding import max_over_ranks
+            t_e2e = max_over_ranks(t_e2e)
+        e2e = {"value": job_flops * e2e_steps / t_e2e / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": a.nbytes + Nl * cs.K,
+               "d2h_bytes_per_step": cs.M * Nl * y_h[0].element_size(), "steps": e2e_steps,
                "chunks": args.e2e_chunks, "pipelined_streams": lanes,
                "api": "scaled_mm_host (emu_scaled_mm_host)"}
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and not args.no_cpu_baseline:
-        v, cores, sample = oracle_rate(cs, a, b, args.cpu_seconds)
+        v, cores, sample, parity = oracle_leg(cs, a, b, args.cpu_seconds, got)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
         config = config_dict(cs, "flushed between timed steps (256 MiB write)")
-        config["tile"] = api.tile_for(cs.M, cs.N, cs.K, use_fast_accum=cs.fast_accum,
+        config["tile"] = api.tile_for(cs.M, Nl or cs.N, cs.K, use_fast_accum=cs.fast_accum,
                                       splitk=cs.split_S, preset=cs.preset)
+        if ws > 1:
+            config["parallelism"] = (f"{ws} replicas" if args.shard == "replicas"
+                                     else f"{ws} column slabs of N")
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "scaling": "weak" if args.shard == "replicas" else "strong",
+                "vs_baseline": None, "dtype": dtype_label(cs),
                 "data": "synthetic",
                 "config": config,
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "cpu_baseline": cpu, "parity": parity, "e2e": e2e,
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "wall_s_timed_region": wall}
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+    if parity is not None and parity["mismatches"]:
+        sys.exit(f"parity: {parity['mismatches']} of {parity['checked']} outputs differ from the oracle")
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="linear")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--shard", default="replicas", choices=("replicas", "columns"),
+                    help="N > 1: whole workload per rank (weak) or column slabs of it (strong)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--e2e-chunks", type=int, default=1,
                     help="column slabs of the host-buffer call (copies overlap the GEMM)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the GEMM kernel from an ncu capture")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle leg (and with it the parity check)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -281,7 +281,11 @@ int emu_preset_get(const char* name, emu_preset_t* out) {
 
 size_t emu_workspace_bytes(int64_t M, int64_t N, int32_t split_S) {
   if (M < 0 || N < 0 || split_S < 1) return 0;
-  if (split_S == 1) return 0;
+  if (split_S == 1 || M == 0 || N == 0) return 0;
+  // S * M * N * 4, rounded up to 256, or SIZE_MAX when that does not fit in size_t
+  // (checked by division before multiplying, so no product wraps)
+  const size_t lim = (SIZE_MAX - 255) / sizeof(float);
+  if ((size_t)M > lim / (size_t)N || (size_t)M * (size_t)N > lim / (size_t)split_S) return SIZE_MAX;
   const size_t b = (size_t)split_S * (size_t)M * (size_t)N * sizeof(float);
   return (b + 255) & ~(size_t)255;
 }
@@ -588,6 +592,10 @@ int emu_scaled_mm_noalloc(const uint8_t* A, emu_fp8_t fmt_a, const uint8_t* B, e
                           int32_t fast_accum, int32_t split_S, const emu_preset_t* preset,
                           void* stream) {
   g_last_error.clear();
+  // the checks and statuses of emu_scaled_mm first, then the static scratch's limit
+  const int rc = check_args(fmt_a, fmt_b, M, N, K, false, out_dtype, split_S, preset);
+  if (rc != EMU_OK) return rc;
+  if (M == 0 || N == 0) return EMU_OK;
   const size_t need = emu_workspace_bytes(M, N, split_S);
   if (need > EMU_NOALLOC_SCRATCH_BYTES)
     return fail(EMU_EUNSUPPORTED,

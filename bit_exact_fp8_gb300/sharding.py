@@ -9,7 +9,7 @@ of the output slabs, for callers that need the whole output on every rank.
 """
 from __future__ import annotations
 
-from typing import Optional, Tuple
+from typing import Callable, Optional, Tuple
 
 import torch
 
@@ -65,16 +65,23 @@ def gather_columns(local: torch.Tensor, N: int, group=None) -> torch.Tensor:
 
 def scaled_mm_column_sharded(mat1: torch.Tensor, mat2: torch.Tensor, scale_a: torch.Tensor,
                              scale_b: torch.Tensor, *, group=None, gather: bool = True,
+                             compute: Optional[Callable[..., torch.Tensor]] = None,
                              **kwargs) -> torch.Tensor:
     """This rank's share of ``scaled_mm(mat1, mat2, ...)``: its column slab of the
-    output, computed on its own GPU; with ``gather`` the full output on every rank."""
+    output, computed on its own GPU; with ``gather`` the full output on every rank.
+
+    ``compute`` is the per-rank GEMM, called as ``compute(mat1, mat2_slab, scale_a,
+    scale_b, **kwargs)`` with the [K, n1 - n0] column-major slab of mat2; it defaults
+    to ``api.scaled_mm`` (the CUDA path).  Another GEMM of the same argument set can
+    stand in for it, e.g. on hosts without a GPU."""
     import torch.distributed as dist
-    from .api import scaled_mm
+    if compute is None:
+        from .api import scaled_mm as compute
     world = dist.get_world_size(group) if dist.is_initialized() else 1
     rank = dist.get_rank(group) if dist.is_initialized() else 0
     N = mat2.shape[1]
     n0, n1 = column_slab(N, rank, world)
-    local = scaled_mm(mat1, mat2[:, n0:n1], scale_a, scale_b, **kwargs)
+    local = compute(mat1, mat2[:, n0:n1], scale_a, scale_b, **kwargs)
     if not gather or world == 1:
         return local
     return gather_columns(local, N, group)

@@ -48,8 +48,10 @@ extern "C" {
 #define EMU_EREJECT (-2)       /* a call torch 2.7.1 / cuBLAS rejects ("Limitations of mmaemu
                                   v0.1", table "Features outside v0.1": e5m2 x e5m2, K or N not a
                                   multiple of 16, storage not 16-byte aligned)                  */
-#define EMU_EUNSUPPORTED (-3)  /* outside the modelled scope: bias, row-wise scales, fp8 output,
-                                  a preset the kernels do not implement                        */
+#define EMU_EUNSUPPORTED (-3)  /* outside the modelled scope: scale_result with a non-FP8
+                                  output, split_S above 64, a preset the kernels do not
+                                  implement (bias and row-wise scales have no argument here:
+                                  the Python layer raises for them)                            */
 #define EMU_ECUDA (-4)         /* a CUDA launch error (cudaGetLastError)                        */
 
 /* FP8 operand formats (OCP): E4M3FN (bias 7, no Inf, S.1111.111 = NaN) and E5M2
@@ -83,8 +85,9 @@ typedef struct {
 int emu_preset_get(const char* name, emu_preset_t* out);
 
 /* Bytes of device workspace emu_scaled_mm needs for these sizes: S * M * N * 4
-   rounded up to 256 for split_S > 1 (the fp32 split partials), 0 for split_S == 1.
-   Returns 0 for invalid sizes. */
+   rounded up to 256 for split_S > 1 (the fp32 split partials), 0 for split_S == 1
+   or an empty output.  Returns 0 for invalid sizes, and SIZE_MAX when the product
+   does not fit in size_t (no workspace can then be large enough). */
 size_t emu_workspace_bytes(int64_t M, int64_t N, int32_t split_S);
 
 /*

@@ -18,24 +18,36 @@ def lib():
     return _lib
 
 
-def declared_functions():
-    names = set()
-    inc = os.path.join(ROOT, "include")
-    for f in os.listdir(inc):
-        if f.endswith(".h"):
-            src = open(os.path.join(inc, f)).read()
-            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-            names |= set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(emu_\w+)\s*\(", src, flags=re.M))
-    return names
+def declared_functions(header):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(emu_\w+)\s*\(", src, flags=re.M))
+
+
+def test_headers_are_the_two_libraries():
+    assert sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")) == \
+        ["emu_fp8.h", "emu_peaks.h"]
 
 
 def test_library_exports_every_declared_symbol(lib):
     L = lib.load()
-    declared = declared_functions()
+    declared = declared_functions("emu_fp8.h")
     assert {"emu_scaled_mm", "emu_workspace_bytes", "emu_preset_get"} <= declared
     for name in declared:
         assert hasattr(L, name), name
     assert set(lib.EXPORTED) == declared
+
+
+def test_peaks_library_exports_every_declared_symbol(lib):
+    from bit_exact_fp8_gb300 import peaks
+    L = peaks.load()
+    declared = declared_functions("emu_peaks.h")
+    assert declared == {"emu_peaks_count", "emu_peaks_name", "emu_peaks_measure",
+                        "emu_peaks_f32x2_agreement"}
+    for name in declared:
+        assert hasattr(L, name), name
+    assert L.emu_peaks_count() == 13
+    assert L.emu_peaks_name(12) == b"emulation_mix_macs" and L.emu_peaks_name(13) == b""
 
 
 def test_presets_and_abi(lib):
@@ -192,3 +204,48 @@ def test_python_host_api_rejects_device_and_bad_dtypes():
         scaled_mm_host(x.float(), w.t(), 1.0, 1.0)
     with pytest.raises(ValueError):
         scaled_mm_host(x, w, 1.0, 1.0)                          # [16,32] @ [16,32]
+
+
+def test_workspace_bytes_never_wraps(lib):
+    # S * M * N * 4 beyond size_t: SIZE_MAX, so no workspace passes the size check
+    big = (1 << 31) - 1
+    assert lib.emu_workspace_bytes(big, big, 64) == (1 << 64) - 1
+    assert lib.emu_workspace_bytes(1 << 30, 1 << 30, 64) == (1 << 64) - 1
+    assert lib.emu_workspace_bytes(1 << 20, 1 << 20, 64) == 64 * (1 << 40) * 4
+    assert lib.emu_workspace_bytes(0, 1 << 30, 64) == 0
+    st = call(lib, M=big, N=big - 15, split_S=64, workspace=FAKE, workspace_bytes=1 << 40)
+    assert st == -1 and "workspace" in lib.emu_last_error()
+
+
+def _noalloc(lib, **kw):
+    args = dict(A=FAKE, fmt_a=0, B=FAKE, fmt_b=0, M=16, N=64, K=256, scale_a=FAKE,
+                scale_b=FAKE, out=FAKE, out_dtype=1, fast_accum=1, split_S=2,
+                preset=lib.emu_preset_get("hopper"), stream=0)
+    args.update(kw)
+    return lib.emu_scaled_mm_noalloc(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(fmt_a=1, fmt_b=1), -2),                 # e5m2 x e5m2: EREJECT, as emu_scaled_mm
+    (dict(K=250), -2),                            # K not a multiple of 16
+    (dict(fmt_a=2), -1),                          # unknown format
+    (dict(split_S=0), -1),
+])
+def test_noalloc_argument_statuses_come_before_the_scratch_limit(lib, kw, status):
+    # the same statuses as emu_scaled_mm, even when the partials would not fit the
+    # static scratch (S * M * N far above EMU_NOALLOC_SCRATCH_BYTES / 4)
+    assert _noalloc(lib, M=1 << 20, N=1 << 20, **kw) == status
+    assert _noalloc(lib, **kw) == status
+
+
+def test_noalloc_scratch_limit_is_exact(lib):
+    # one 16-column step above S * M * N = EMU_NOALLOC_SCRATCH_BYTES / 4 is refused on
+    # the host (nothing touches a GPU); the exact fill itself runs in the GPU test
+    limit = lib.EMU_NOALLOC_SCRATCH_BYTES // 4
+    S, M = 2, 16
+    N = limit // (S * M)
+    assert S * M * N == limit
+    assert lib.emu_workspace_bytes(M, N, S) == lib.EMU_NOALLOC_SCRATCH_BYTES
+    assert _noalloc(lib, M=M, N=N + 16, split_S=S) == -3
+    assert "static scratch" in lib.emu_last_error()
+    assert _noalloc(lib, M=0, N=N + 16, split_S=S) == 0       # empty output: nothing to do

@@ -40,6 +40,34 @@ def sampled_check(cs, count=256):
 
 # ---------------------------------------------------------------------------
 # the five workloads
+_INPUTS = {}
+
+
+def inputs(cs):
+    """The case's operands, drawn once per recipe (the variants of a workload share them)."""
+    key = (cs.M, cs.N, cs.K, cs.fmt_a, cs.fmt_b, cs.gen, cs.seed, cs.sigma_a, cs.sigma_b)
+    if key not in _INPUTS:
+        _INPUTS[key] = W.make_inputs(cs)
+    return _INPUTS[key]
+
+
+def all_indices(M, N):
+    im, jn = np.meshgrid(np.arange(M, dtype=np.int64), np.arange(N, dtype=np.int64), indexing="ij")
+    return im.ravel(), jn.ravel()
+
+
+def stripe_check(cs, got, a, b, rows, cols):
+    """A full-size row stripe and column stripe of the output against the oracle."""
+    import oracle
+    kw = dict(scale_result=cs.scale_result)
+    want = oracle.scaled_mm(a[rows], b, cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
+                            cs.fast_accum, cs.split_S, cs.preset, **kw)
+    assert_bits_equal(got[rows], want, f"{cs.name} rows {rows.start}:{rows.stop}")
+    want = oracle.scaled_mm(a, b[cols], cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
+                            cs.fast_accum, cs.split_S, cs.preset, **kw)
+    assert_bits_equal(got[:, cols], want, f"{cs.name} cols {cols.start}:{cols.stop}")
+
+
 def test_tiny_full():
     full_check(W.case("tiny"))
 
@@ -55,14 +83,35 @@ def test_square_ragged_full(cs):
     full_check(W.shrink(cs, 200, 144, 1040))
 
 
-@pytest.mark.parametrize("cs", W.CONFIGS["square"][::2], ids=lambda c: c.name)
-def test_square_full_size_sampled(cs):
-    sampled_check(cs, count=96)
+@pytest.mark.parametrize("i,cs", list(enumerate(W.CONFIGS["square"])), ids=lambda x: getattr(x, "name", str(x)))
+def test_square_full_size_stripes(i, cs):
+    # 64 full rows and 64 full columns at offsets that straddle CTA tiles (about 1e9
+    # MACs each for the oracle), plus sampled outputs anywhere
+    a, b = inputs(cs)
+    got = gpu_run(cs, a, b)
+    r0, c0 = 1000 + 517 * i, 3000 - 389 * i
+    stripe_check(cs, got, a, b, slice(r0, r0 + 64), slice(c0, c0 + 64))
+    im, jn = sample_indices(cs.M, cs.N, 96, seed=i)
+    assert_bits_equal(got[im, jn], oracle_sampled(cs, a, b, im, jn), cs.name + " (sampled)")
+
+
+_SPLITK_ACC = {}
 
 
 @pytest.mark.parametrize("cs", W.CONFIGS["splitk"], ids=lambda c: c.name)
-def test_splitk_full_size_sampled(cs):
-    sampled_check(cs, count=64)
+def test_splitk_full_size_every_output(cs):
+    # all 16 x 256 outputs at K = 262144: the oracle's accumulators are computed once
+    # per (preset, S, accumulation) and go through the epilogue of each output dtype
+    import oracle
+    a, b = inputs(cs)
+    got = gpu_run(cs, a, b)
+    key = (cs.preset, cs.split_S, cs.fast_accum)
+    if key not in _SPLITK_ACC:
+        im, jn = all_indices(cs.M, cs.N)
+        _SPLITK_ACC[key] = oracle.acc_sampled(a, b, cs.fmt_a, cs.fmt_b, im, jn, cs.fast_accum,
+                                              cs.split_S, cs.preset)
+    want = oracle.epilogue(_SPLITK_ACC[key], cs.scale_a, cs.scale_b, cs.out_dtype)
+    assert_bits_equal(got, want.reshape(cs.M, cs.N), cs.name)
 
 
 @pytest.mark.parametrize("cs", [c for c in W.CONFIGS["splitk"] if c.out_dtype == "f32"],
@@ -72,10 +121,41 @@ def test_splitk_ragged_full(cs):
     full_check(W.shrink(cs, 16, 64, 16384 + 48))
 
 
-@pytest.mark.parametrize("cs", W.CONFIGS["projection"], ids=lambda c: c.name)
-def test_projection_sampled_and_ragged(cs):
-    sampled_check(cs, count=128)
+@pytest.mark.parametrize("i,cs", list(enumerate(W.CONFIGS["projection"])), ids=lambda x: getattr(x, "name", str(x)))
+def test_projection_full_size_stripes_and_ragged(i, cs):
+    a, b = inputs(cs)
+    got = gpu_run(cs, a, b)
+    r0, c0 = 4100 - 37 * i, 1000 + 21 * i
+    stripe_check(cs, got, a, b, slice(r0, r0 + 64), slice(c0, c0 + 64))
+    im, jn = sample_indices(cs.M, cs.N, 128, seed=i)
+    assert_bits_equal(got[im, jn], oracle_sampled(cs, a, b, im, jn), cs.name + " (sampled)")
     full_check(W.shrink(cs, 272, 208, 1920))
+
+
+# the fp32 accumulator entry point ("User guide", section 3: both operands as
+# [rows, K]; the accumulator before the scales): every output against the oracle's
+# accumulator, NaN rows and columns included
+@pytest.mark.parametrize("fast", (True, False))
+@pytest.mark.parametrize("S,preset", ((1, "hopper"), (2, "hopper"), (3, "ada")))
+def test_accumulate_is_the_oracle_accumulator(fast, S, preset):
+    import oracle
+    from bit_exact_fp8_gb300 import accumulate
+    cs = W.Case("acc", 40, 96, 1040, out_dtype="f32", fast_accum=fast, split_S=S, preset=preset,
+                gen="mixed", seed=13)
+    a, b = W.make_inputs(cs)
+    a[3, 77] = 0x7F                      # NaN code in row 3
+    b[5, 500] = 0xFF                     # NaN code in column 5
+    dev = torch.device("cuda:0")
+    x = torch.from_numpy(a).to(dev).view(torch.float8_e4m3fn)
+    w = torch.from_numpy(b).to(dev).view(torch.float8_e4m3fn)
+    got = accumulate(x, w, fast, splitk=S, preset=preset)
+    torch.cuda.synchronize()
+    got = got.cpu().view(torch.int32).numpy().view(np.uint32)
+    im, jn = all_indices(cs.M, cs.N)
+    want = oracle.acc_sampled(a, b, cs.fmt_a, cs.fmt_b, im, jn, fast, S, preset).reshape(cs.M, cs.N)
+    assert_bits_equal(got, want, f"accumulate fast={fast} S={S} {preset}")
+    assert (got[3] == 0x7FC00000).all() and (got[:, 5] == 0x7FC00000).all()
+    assert not (got == 0x80000000).any()          # the accumulator is never -0
 
 
 # ---------------------------------------------------------------------------

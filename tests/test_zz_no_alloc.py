@@ -4,10 +4,11 @@ start-up, a host framework that owns every allocation).  It keeps the split-K
 partials in the library's static device scratch instead of a caller workspace.
 
 Called through the C ABI binding, it must return the same bits as emu_scaled_mm
-with a caller-allocated workspace (bit-exact, the tolerance of every parity test
-here) on two calls in a row, since each call reuses the scratch the previous call
-left behind.  This file is collected last, and passes alone in a fresh process as
-well as after the other tests."""
+with a caller-allocated workspace, and as the CPU oracle (bit-exact, the tolerance
+of every parity test here), on two calls in a row, since each call reuses the
+scratch the previous call left behind.  One case fills the scratch exactly
+(split_S * M * N == EMU_NOALLOC_SCRATCH_BYTES / 4).  This file is collected last,
+and passes alone in a fresh process as well as after the other tests."""
 import numpy as np
 import pytest
 import torch
@@ -40,6 +41,8 @@ CASES = [
     W.shrink(W.case("splitk-hopper-S2-slow-f32"), 48, 112, 4096 + 16),
     W.case("splitk-ada-S24-fast-f32"),                       # full size, 393 KB of partials
     W.case("tiny"),                                          # S = 1: no scratch at all
+    # the partials fill the 4 MiB scratch exactly: 2 x 16 x 32768 fp32
+    W.shrink(W.case("splitk-hopper-S2-fast-bf16"), 16, 32768, 2048),
 ]
 
 
@@ -64,6 +67,12 @@ def test_noalloc_matches_workspace_entry_point_twice(lib, cs):
                            stream)
     assert st == 0, lib.emu_last_error()
     want = _bits(ref)
+    import oracle
+    orc = oracle.scaled_mm(a, b, cs.fmt_a, cs.fmt_b, cs.scale_a, cs.scale_b, cs.out_dtype,
+                           cs.fast_accum, cs.split_S, cs.preset)
+    orc = orc.view(np.int32 if cs.out_dtype == "f32" else np.int16)
+    bad = np.flatnonzero(orc.ravel() != want.ravel())
+    assert bad.size == 0, f"emu_scaled_mm vs oracle: {bad.size} outputs differ, first at {bad[:5]}"
 
     for call in range(2):
         out = torch.empty((cs.M, cs.N), dtype=odt, device=dev)

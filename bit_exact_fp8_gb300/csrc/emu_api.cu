@@ -56,7 +56,7 @@ struct TileInfo {
   const char* name;
   int tm, tn, bm, bn, threads;
   int resident, resident_slow;  // CTAs per SM (shared memory and the register budget)
-  int bk, g;
+  int bk, g;                    // chain tiles: bk of 32-product blocks (16-product: 64)
   // cost model, both fitted to GB300 measurements (SM clocks per K element) on the
   // benchmark workloads and on M = 1 .. 512 at N = 5760, K = 1920:
   double ipm;                   // effective thread instructions per MAC at full load
@@ -75,8 +75,26 @@ constexpr TileInfo kTiles[] = {
     {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, false},
     {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 35.0, 18.0, 1.0, true},
     {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 26.0, 21.0, 1.0, true},
+    // chain tiles (emu_chain_kernel): one output per lane group of g lanes
+    {"C2", 1, 1, 8, 8, 128, 2, 2, 128, 2, 1e9, 1e9, 1.0, false},
+    {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 1e9, 1e9, 1.0, false},
+    {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 1e9, 1e9, 1.0, false},
+    {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 1e9, 1e9, 1.0, false},
+    // large tiles with two blocks per 64-code stage (the second block's pass 1 runs
+    // inside the first block's pass 2), one CTA per SM
+    {"M64K", 4, 4, 64, 64, 256, 1, 1, 64, 1, 1e9, 1e9, 1.0, false},
+    {"M128", 4, 4, 128, 64, 512, 1, 1, 64, 1, 1e9, 1e9, 1.0, false},
+    // M64 and M32 with the labels of the next stage decoded a stage ahead
+    {"M64A", 4, 4, 64, 64, 256, 2, 1, 32, 1, 1e9, 1e9, 1.0, false},
+    {"M32A", 4, 4, 64, 32, 128, 3, 3, 32, 1, 1e9, 1e9, 1.0, false},
 };
-constexpr int kNumTiles = 8;
+constexpr int kNumTiles = 16;
+constexpr int kFirstChainTile = 8;
+// K-stage of a tile for blocks of blk products (the chain tiles stage 64 codes for
+// 16-product blocks)
+int tile_bk(int t, int blk) {
+  return (t >= kFirstChainTile && t < kFirstChainTile + 4 && blk == 16) ? 64 : kTiles[t].bk;
+}
 // SMs of the current device (152 on a GB300), cached per device (atomics: the entry
 // points may be called from several host threads)
 int sm_count() {
@@ -134,10 +152,14 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_
   return EMU_OK;
 }
 
-template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, int G, int MINB, bool PK>
+template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, int G, int MINB, bool PK,
+          bool LA = false, int LREP = 1>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
-  using TS = emu::TileShape<TM, TN, WM, WN, BK, G>;
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK>;
+  using TS = emu::TileShape<TM, TN, WM, WN, BK, G, LREP>;
+  // the resident CTAs the register budget is set for also fit in shared memory
+  // (228 KB per SM, 1 KB of it reserved per CTA)
+  static_assert(MINB * (TS::SMEM_BYTES + 1024) <= 228 * 1024, "resident CTAs fit in shared memory");
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK, LA, LREP>;
   // the dynamic shared memory limit is a per-function, per-device attribute; setting
   // it twice (two host threads racing on the first call) is harmless
   static std::atomic<bool> configured[64];
@@ -168,20 +190,60 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
 // MINB, MINB_SLOW: the CTAs per SM the fast and slow variants are meant to keep
 // resident (the register budget ptxas is held to)
 template <int TM, int TN, int WM, int WN, int BK, int G, int MINB, int MINB_SLOW = MINB,
-          bool PK = true>
+          bool PK = true, bool LA = false, int LREP = 1>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, G, MINB_SLOW, PK>(p, st)
-                : launch_one<TM, TN, WM, WN, BK, 32, false, G, MINB, PK>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, G, MINB_SLOW, PK, LA, LREP>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, G, MINB, PK, LA, LREP>(p, st);
   }
-  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, G, MINB_SLOW, PK>(p, st)
-              : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK>(p, st);
+  // 16-product blocks take the tile without labels ahead (it needs one block per stage)
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, G, MINB_SLOW, PK, false, LREP>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK, false, LREP>(p, st);
+}
+
+template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB>
+int launch_chain_one(const emu::GemmParams& p, cudaStream_t st) {
+  using CS = emu::ChainShape<BM, BN, G, BK, BLK, LREP>;
+  auto kern = emu::emu_chain_kernel<BM, BN, G, BK, BLK, SLOW, LREP, MINB>;
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::SMEM_BYTES);
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  CUtensorMap tmA, tmB;
+  int rc = make_operand_map(&tmA, p.A, p.M, p.K, BM, BK, false);
+  if (rc != EMU_OK) return rc;
+  rc = make_operand_map(&tmB, p.B, p.N, p.K, BN, BK, false);
+  if (rc != EMU_OK) return rc;
+  const int64_t tiles_m = (p.M + BM - 1) / BM;
+  for (int64_t y0 = 0; y0 < tiles_m; y0 += 65535) {
+    emu::GemmParams q = p;
+    q.m_tile0 = y0;
+    const int64_t ny = tiles_m - y0 < 65535 ? tiles_m - y0 : 65535;
+    dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)ny, (unsigned)p.S);
+    kern<<<grid, CS::NT, CS::SMEM_BYTES, st>>>(q, tmA, tmB);
+  }
+  return EMU_OK;
+}
+
+// chain tile BM x BN outputs, G lanes each: 128-code stages for 32-product blocks,
+// 64-code stages for 16-product blocks
+template <int BM, int BN, int G, int LREP, int MINB>
+int launch_chain(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
+  if (blk == 32) {
+    return slow ? launch_chain_one<BM, BN, G, 128, 32, true, LREP, MINB>(p, st)
+                : launch_chain_one<BM, BN, G, 128, 32, false, LREP, MINB>(p, st);
+  }
+  return slow ? launch_chain_one<BM, BN, G, 64, 16, true, LREP, MINB>(p, st)
+              : launch_chain_one<BM, BN, G, 64, 16, false, LREP, MINB>(p, st);
 }
 
 // Pick the tile with the lowest estimated time per K element, in SM clocks: the
 // larger of the issue time of the CTAs an SM receives and the latency-bound time of
 // its waves of resident CTAs.  EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
-int choose_tile(const emu::GemmParams& p, bool slow, double sms) {
+int choose_tile(const emu::GemmParams& p, int blk, bool slow, double sms) {
   static const int forced = [] {         // read once (thread-safe static initialisation)
     const char* env = getenv("EMU_FP8_TILE");
     if (env)
@@ -189,7 +251,7 @@ int choose_tile(const emu::GemmParams& p, bool slow, double sms) {
         if (std::strcmp(env, kTiles[t].name) == 0) return t;
     return -1;
   }();
-  auto usable = [&](int t) { return p.S == 1 || p.ktile % kTiles[t].bk == 0; };
+  auto usable = [&](int t) { return p.S == 1 || p.ktile % tile_bk(t, blk) == 0; };
   if (forced >= 0 && usable(forced)) return forced;
   auto ctas_of = [&](const TileInfo& ti) {
     return (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
@@ -210,16 +272,32 @@ int choose_tile(const emu::GemmParams& p, bool slow, double sms) {
   return best;
 }
 
+// decode-table copies per tile (the lanes sharing a copy, 32 / LREP, contend for its banks);
+// the residency each tile is built for bounds them through its shared memory
+#ifndef EMU_LREP
+#define EMU_LREP 8
+#endif
+constexpr int LREP_M40 = EMU_LREP, LREP_M32 = EMU_LREP, LREP_M64 = EMU_LREP, LREP_S = 2,
+              LREP_K = 2;
+
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
-  switch (choose_tile(p, slow, sm_count())) {
-    case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1>(p, blk, slow, st);
-    case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3>(p, blk, slow, st);
-    case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6>(p, blk, slow, st);
-    case 3: return launch_tile<1, 2, 4, 4, 64, 8, 8, 8, false>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 8, 64, 4, 8, 8, false>(p, blk, slow, st);
-    case 5: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1>(p, blk, slow, st);
-    case 6: return launch_tile<1, 2, 4, 4, 128, 8, 7, 7, false>(p, blk, slow, st);
-    default: return launch_tile<1, 2, 4, 8, 128, 4, 4, 4, false>(p, blk, slow, st);
+  switch (choose_tile(p, blk, slow, sm_count())) {
+    case 8: return launch_chain<8, 8, 2, 32, 2>(p, blk, slow, st);
+    case 9: return launch_chain<8, 4, 4, 32, 2>(p, blk, slow, st);
+    case 10: return launch_chain<8, 8, 1, 8, 4>(p, blk, slow, st);
+    case 11: return launch_chain<16, 16, 1, 8, 2>(p, blk, slow, st);
+    case 12: return launch_tile<4, 4, 16, 16, 64, 1, 1, 1, true, false, 8>(p, blk, slow, st);
+    case 13: return launch_tile<4, 4, 32, 16, 64, 1, 1, 1, true, false, 8>(p, blk, slow, st);
+    case 14: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1, true, true, LREP_M64>(p, blk, slow, st);
+    default: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, true, LREP_M32>(p, blk, slow, st);
+    case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1, 1, true, false, LREP_M40>(p, blk, slow, st);
+    case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, false, LREP_M32>(p, blk, slow, st);
+    case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6, 6, true, false, LREP_S>(p, blk, slow, st);
+    case 3: return launch_tile<1, 2, 4, 4, 64, 8, 8, 8, false, false, LREP_K>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 8, 64, 4, 8, 8, false, false, LREP_K>(p, blk, slow, st);
+    case 5: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1, true, false, LREP_M64>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, 8, 7, 7, false, false, LREP_K>(p, blk, slow, st);
+    case 7: return launch_tile<1, 2, 4, 8, 128, 4, 4, 4, false, false, LREP_K>(p, blk, slow, st);
   }
 }
 
@@ -642,7 +720,8 @@ int emu_tile_for(int64_t M, int64_t N, int64_t K, int32_t fast_accum, int32_t sp
     const emu::GemmParams p = make_params(nullptr, EMU_E4M3FN, nullptr, EMU_E4M3FN, M, N, K,
                                           nullptr, nullptr, nullptr, nullptr, EMU_OUT_F32,
                                           split_S, preset, nullptr);
-    t = kTiles[choose_tile(p, fast_accum == 0, sms > 0 ? (double)sms : (double)sm_count())].name;
+    t = kTiles[choose_tile(p, preset->block_width, fast_accum == 0,
+                           sms > 0 ? (double)sms : (double)sm_count())].name;
   }
   if (std::strlen(t) + 1 > name_len) return fail(EMU_EINVAL, "name buffer of %zu bytes is too small", name_len);
   std::strcpy(name, t);

@@ -245,6 +245,18 @@ __device__ __forceinline__ void decode_code(uint32_t code, int fmt, int pre, flo
   lab = sig ? ((elab + kLabBias) << 7) : kZeroLab;
 }
 
+// One decode-table entry per code: the pre-scaled value's bits 31..20 (sign, exponent,
+// at most three fraction bits, NaN and Inf included) and the 16-bit label in bits 15..0.
+// The tables hold LREP copies of every entry, interleaved (entry e of copy r at word
+// e * LREP + r), and lane l reads copy l % LREP, so that the lanes of a warp spread
+// their random lookups over the banks.
+__device__ __forceinline__ uint32_t lut_entry(uint32_t code, int fmt, int pre) {
+  float v;
+  int lab;
+  decode_code(code, fmt, pre, v, lab);
+  return (__float_as_uint(v) & 0xFFF00000u) | ((uint32_t)lab & 0xFFFFu);
+}
+
 // N consecutive 32-bit words from shared memory, p aligned to 4 * (N & -N) bytes,
 // in the widest loads that alignment allows
 template <int N>
@@ -280,8 +292,9 @@ __device__ __forceinline__ uint32_t c16_hi(float c) { return __float_as_uint(c) 
 // adjacent lanes share one thread tile and take every G-th k-pair (pass 1) and
 // product (pass 2) of each block; their partial block maxima and partial sums are
 // combined with warp shuffles (exact), so all G lanes hold the same chain state.
-template <int TM, int TN, int WM, int WN, int BK_, int G = 1>
+template <int TM, int TN, int WM, int WN, int BK_, int G = 1, int LREP_ = 1>
 struct TileShape {
+  static constexpr int LREP = LREP_;                 // decode-table copies
   static constexpr int NT = WM * WN * G;
   static constexpr int BM = WM * TM;
   static constexpr int BN = WN * TN;
@@ -315,7 +328,7 @@ struct TileShape {
   static constexpr int B_LAB = B_VAL + (BK * BN + (BK / 16) * PAD) * 4;
   static constexpr int STAGE_BYTES = ((B_LAB + (BK / 2 * BN + (BK / 16) * PAD) * 4) + 127) / 128 * 128;
   static constexpr int STAGE_OFF = NS * RAW_STAGE;
-  static constexpr int LUT_BYTES = 2 * 256 * 8;
+  static constexpr int LUT_BYTES = 2 * 256 * LREP * 4;
   static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
   static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
   // dynamic shared memory to request: the layout plus room to align its base
@@ -324,11 +337,11 @@ struct TileShape {
 };
 
 template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, int G, int MINB,
-          bool PK>
+          bool PK, bool LA = false, int LREP = 1>
 __global__ void __launch_bounds__(WM * WN * G, MINB)
 emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB) {
-  using TS = TileShape<TM, TN, WM, WN, BK_, G>;
+  using TS = TileShape<TM, TN, WM, WN, BK_, G, LREP>;
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "lane groups of 1, 2, 4 or 8");
   static_assert(BLK % G == 0, "a block's products are dealt evenly to the group");
   static_assert(BLK % (2 * G) == 0, "a block's k-pairs are dealt evenly to the group");
@@ -360,8 +373,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // layout base: the dynamic buffer rounded up to the raw ring's alignment
   unsigned char* const smem =
       smem_dyn + ((TS::RAW_ALIGN - (smem_u32(smem_dyn) & (TS::RAW_ALIGN - 1))) & (TS::RAW_ALIGN - 1));
-  uint2* lutA = reinterpret_cast<uint2*>(smem + TS::LUT_OFF);
-  uint2* lutB = lutA + 256;
+  uint32_t* lutA = reinterpret_cast<uint32_t*>(smem + TS::LUT_OFF);
+  uint32_t* lutB = lutA + 256 * LREP;
   const uint32_t bar0 = smem_u32(smem + TS::BAR_OFF);
 
   const int tid = threadIdx.x;
@@ -372,12 +385,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int s = blockIdx.z;
 
   // decode tables: code -> (pre-scaled value bits, label) for each operand
-  for (int c = tid; c < 256; c += NT) {
-    float v; int lab;
-    decode_code((uint32_t)c, p.fmt_a, kPreA, v, lab);
-    lutA[c] = make_uint2(__float_as_uint(v), (uint32_t)lab & 0xFFFFu);
-    decode_code((uint32_t)c, p.fmt_b, kPreB, v, lab);
-    lutB[c] = make_uint2(__float_as_uint(v), (uint32_t)lab & 0xFFFFu);
+  for (int i = tid; i < 256 * LREP; i += NT) {
+    lutA[i] = lut_entry((uint32_t)(i / LREP), p.fmt_a, kPreA);
+    lutB[i] = lut_entry((uint32_t)(i / LREP), p.fmt_b, kPreB);
   }
 
   // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
@@ -419,8 +429,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     tma_load_2d(dst, &tmA, k, (int)m0, bar);
     tma_load_2d(dst + TS::RAW_A, &tmB, k, (int)n0, bar);
   };
-  // the decoder threads: decode the raw slot of stage st into operand buffer buf
-  auto decode_stage = [&](int64_t st, int buf) {
+  // the decoder threads: decode the raw slot of stage st into operand buffer buf;
+  // what: 1 values, 2 labels, 3 both
+  auto decode_stage = [&](int64_t st, int buf, int what) {
     const unsigned char* raw = smem + (int)(st % NS) * TS::RAW_STAGE;
     unsigned char* base = smem + TS::STAGE_OFF + buf * TS::STAGE_BYTES;
     float* sAv = reinterpret_cast<float*>(base + TS::A_VAL);
@@ -437,6 +448,8 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       return *reinterpret_cast<const uint4*>(raw + off_row + hs * 16);
     };
     const int warp = tid / 32;
+    const uint32_t* lA = lutA + (tid % 32) % LREP;        // this lane's table copies
+    const uint32_t* lB = lutB + (tid % 32) % LREP;
     const bool decoder = NDEC == NT || warp % 4 >= XW;
     const int dt = NDEC == NT ? tid : ((warp / 4) * (4 - XW) + warp % 4 - XW) * 32 + tid % 32;
 #pragma unroll
@@ -449,15 +462,19 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
-          const uint2 d0 = lutA[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
-          const uint2 d1 = lutA[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3))];
-          if (PK) {
-            *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = make_uint2(d0.x, d1.x);
-          } else {
-            sAv[(h * 16 + j) * BM + h * PAD + row] = __uint_as_float(d0.x);
-            sAv[(h * 16 + j + 1) * BM + h * PAD + row] = __uint_as_float(d1.x);
+          const uint32_t e0 = lA[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3)) * LREP];
+          const uint32_t e1 = lA[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3)) * LREP];
+          const uint2 d0 = make_uint2(e0 & 0xFFF00000u, 0u), d1 = make_uint2(e1 & 0xFFF00000u, 0u);
+          const uint32_t lp = __byte_perm(e0, e1, 0x5410);
+          if (what & 1) {
+            if (PK) {
+              *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = make_uint2(d0.x, d1.x);
+            } else {
+              sAv[(h * 16 + j) * BM + h * PAD + row] = __uint_as_float(d0.x);
+              sAv[(h * 16 + j + 1) * BM + h * PAD + row] = __uint_as_float(d1.x);
+            }
           }
-          sAl[(h * 8 + j / 2) * BM + h * PAD + row] = d0.y | (d1.y << 16);
+          if (what & 2) sAl[(h * 8 + j / 2) * BM + h * PAD + row] = lp;
         }
       } else if (c < A_CHUNKS + B_CHUNKS) {
         const int cb = c - A_CHUNKS;
@@ -467,16 +484,20 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {
-          const uint2 d0 = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3))];
-          const uint2 d1 = lutB[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3))];
-          if (PK) {
-            *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
-                make_uint2(d0.x, d1.x);
-          } else {
-            sBv[(h * 16 + j) * BN + h * PAD + col] = __uint_as_float(d0.x);
-            sBv[(h * 16 + j + 1) * BN + h * PAD + col] = __uint_as_float(d1.x);
+          const uint32_t e0 = lB[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3)) * LREP];
+          const uint32_t e1 = lB[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3)) * LREP];
+          const uint2 d0 = make_uint2(e0 & 0xFFF00000u, 0u), d1 = make_uint2(e1 & 0xFFF00000u, 0u);
+          const uint32_t lp = __byte_perm(e0, e1, 0x5410);
+          if (what & 1) {
+            if (PK) {
+              *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
+                  make_uint2(d0.x, d1.x);
+            } else {
+              sBv[(h * 16 + j) * BN + h * PAD + col] = __uint_as_float(d0.x);
+              sBv[(h * 16 + j + 1) * BN + h * PAD + col] = __uint_as_float(d1.x);
+            }
           }
-          sBl[(h * 8 + j / 2) * BN + h * PAD + col] = d0.y | (d1.y << 16);
+          if (what & 2) sBl[(h * 8 + j / 2) * BN + h * PAD + col] = lp;
         }
       }
     }
@@ -535,10 +556,15 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // block's pass 1 (DPX, integer pipe) inside this block's pass-2 loop (FP32 pipe),
   // so one instruction stream feeds both pipes; the stage's first block runs its
   // own pass 1.
-  constexpr bool kFuse = PK && G == 1 && !SLOW && NBLK >= 2;
+  // LA (labels one stage ahead, tiles with one block per stage): the labels of stage
+  // st + 1 are decoded during stage st - 1, so every block's pass 1 runs inside the
+  // previous block's pass 2, across the stage boundary
+  static_assert(!LA || (NBLK == 1 && PK && G == 1), "labels ahead: one packed block per stage");
+  constexpr bool kFuse = PK && G == 1 && ((!SLOW && NBLK >= 2) || LA);
   uint32_t En[TM][TN];   // the next block's maxima while fused
   // one block of every chain, from the decoded buffer at `base`
-  auto block_step = [&](const unsigned char* base, int k0, bool have_e2, bool fuse_next) {
+  auto block_step = [&](const unsigned char* base, int k0, bool have_e2, bool fuse_next,
+                        const unsigned char* lnext, int k0n) {
     const float* sAv = reinterpret_cast<const float*>(base + TS::A_VAL);
     const float* sBv = reinterpret_cast<const float*>(base + TS::B_VAL);
     if (!have_e2) {
@@ -590,7 +616,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       }
 #pragma unroll
       for (int q = 0; q < BLK / (2 * G); ++q) {
-        if (kFuse && fuse_next) pass1_pair_into(En, base, k0 + BLK, q);
+        if (kFuse && fuse_next) pass1_pair_into(En, lnext, k0n, q);
         const int kp = k0 / 2 + q * G + gl;
         f32x2_t a2[TM], b2[TN];
         if (TM % 2 == 0) {
@@ -675,33 +701,73 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     }
   };
 
-  // decode stage st + 1 into the other buffer while nobody reads it, then one
-  // barrier per stage; thread 0 refills the ring slot everyone has decoded
   bool timed_out = false;
-  if (n_stages > 0) {
-    timed_out = !full_wait(0);
-    decode_stage(0, 0);
-  }
-  if (__syncthreads_or(timed_out)) { give_up(0); return; }
-  if (tid == 0 && NS < n_stages) {
-    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
-    issue(NS);
-  }
-  for (int64_t st = 0; st < n_stages; ++st) {
-    const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
-    // slow chains of the large tiles: the blocks of a stage stay a loop (a restart
-    // may fall after any of them; unrolled, the 64 x 40 tile's 32-product variant
-    // spilled registers); the small tiles unroll them
-#pragma unroll (SLOW && BM * BN > 1024 ? 1 : NBLK)
-    for (int bb = 0; bb < NBLK; ++bb) block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK);
-    if (st + 1 < n_stages) {
-      timed_out = !full_wait(st + 1);
-      decode_stage(st + 1, (int)((st + 1) & 1));
+  if constexpr (LA) {
+    // stage st computes its block from values[st & 1] with the next block's pass 1 on
+    // labels[(st + 1) & 1], decodes the values of st + 1 and the labels of st + 2, then
+    // one barrier; the raw slot of st + 1 is then fully decoded and refilled
+    if (n_stages > 0) {
+      timed_out = !full_wait(0);
+      if (!timed_out) decode_stage(0, 0, 3);
+      if (n_stages > 1 && !timed_out) {
+        timed_out = !full_wait(1);
+        if (!timed_out) decode_stage(1, 1, 2);
+      }
     }
-    if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
-    if (tid == 0 && st + 1 + NS < n_stages) {
+    if (__syncthreads_or(timed_out)) { give_up(0); return; }
+    if (tid == 0 && NS < n_stages) {
       fence_proxy_async();
-      issue(st + 1 + NS);
+      issue(NS);
+    }
+    if (n_stages > 0) {
+      pass1_reset();
+#pragma unroll
+      for (int q = 0; q < BLK / 2; ++q) pass1_pair_into(E2, smem + TS::STAGE_OFF, 0, q);
+    }
+    for (int64_t st = 0; st < n_stages; ++st) {
+      const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
+      const unsigned char* nxt = smem + TS::STAGE_OFF + (int)((st + 1) & 1) * TS::STAGE_BYTES;
+      block_step(cur, 0, true, st + 1 < n_stages, nxt, 0);
+      if (st + 1 < n_stages) decode_stage(st + 1, (int)((st + 1) & 1), 1);
+      if (st + 2 < n_stages) {
+        timed_out = !full_wait(st + 2);
+        if (!timed_out) decode_stage(st + 2, (int)(st & 1), 2);
+      }
+      if (__syncthreads_or(timed_out)) { give_up(st + 2); return; }
+      if (tid == 0 && st + 1 + NS < n_stages) {
+        fence_proxy_async();
+        issue(st + 1 + NS);
+      }
+    }
+  } else {
+    // decode stage st + 1 into the other buffer while nobody reads it, then one
+    // barrier per stage; thread 0 refills the ring slot everyone has decoded
+    if (n_stages > 0) {
+      timed_out = !full_wait(0);
+      decode_stage(0, 0, 3);
+    }
+    if (__syncthreads_or(timed_out)) { give_up(0); return; }
+    if (tid == 0 && NS < n_stages) {
+      fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
+      issue(NS);
+    }
+    for (int64_t st = 0; st < n_stages; ++st) {
+      const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
+      // slow chains of the large tiles: the blocks of a stage stay a loop (a restart
+      // may fall after any of them; unrolled, the 64 x 40 tile's 32-product variant
+      // spilled registers); the small tiles unroll them
+#pragma unroll (SLOW && BM * BN > 1024 ? 1 : NBLK)
+      for (int bb = 0; bb < NBLK; ++bb)
+        block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK, cur, bb * BLK + BLK);
+      if (st + 1 < n_stages) {
+        timed_out = !full_wait(st + 1);
+        decode_stage(st + 1, (int)((st + 1) & 1), 3);
+      }
+      if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
+      if (tid == 0 && st + 1 + NS < n_stages) {
+        fence_proxy_async();
+        issue(st + 1 + NS);
+      }
     }
   }
 
@@ -743,6 +809,336 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       store(p, m * p.N + n, fma_plus0(res[i][j], alpha));
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Chain tiles, for few long chains (the skinny split-K shapes, small M x N): one
+// output per group of G adjacent lanes, BM x BN outputs per CTA.  A block's BLK
+// products are dealt to the group's lanes as contiguous runs of NPL k-pairs.  The
+// work of a block that does not depend on the chain state c -- its exact products
+// and its product-label maximum, group-reduced -- is done one block ahead, while
+// the previous block's c-dependent step (scale from max(E_p, e(c)), truncation,
+// sum, normalise) is in flight; the next stage's decode is dealt over the first
+// NBLK - 1 blocks of the current stage.  Decode tables hold one 32-bit entry per
+// code (the pre-scaled value in bits 31..20, the label in bits 15..0), replicated
+// LREP times so that the lanes of a warp read distinct banks.  Decoded rows (values
+// as k-pairs, labels as k-pair words) are padded by 16 bytes, so that each lane
+// reads its runs from its own base address with compile-time offsets and the rows
+// of a warp start in distinct bank quads.
+template <int BM_, int BN_, int G_, int BK_, int BLK_, int LREP_>
+struct ChainShape {
+  static constexpr int BM = BM_, BN = BN_, G = G_, BK = BK_, BLK = BLK_, LREP = LREP_;
+  static constexpr int GPW = 32 / G;             // lane groups (outputs) per warp
+  static constexpr int WR = G == 4 ? 2 : 4;      // output rows of a warp
+  static constexpr int WC = GPW / WR;            // output columns of a warp
+  static constexpr int NT = BM * BN * G;
+  static constexpr int ROWS = BM + BN;           // operand rows: A rows, then B rows (columns n)
+  static constexpr int KP = BK / 2;              // k-pairs per row and stage
+  static constexpr int NPB = BLK / 2;            // k-pairs per block
+  static constexpr int NPL = NPB / G;            // k-pairs per lane and block
+  static constexpr int NBLK = BK / BLK;
+  static constexpr int RAW_A = BM * BK, RAW_B = BN * BK;
+  static constexpr int RAW_STAGE = (RAW_A + RAW_B + 127) / 128 * 128;
+  // ring depth: about 24 KB of raw stages in flight (4 to 16), so that the TMA round
+  // trip of a stage hides behind the stages before it
+  static constexpr int NS_ = 24576 / RAW_STAGE;
+  static constexpr int NS = NS_ < 4 ? 4 : (NS_ > 16 ? 16 : NS_);
+  static constexpr int VROW = KP * 8 + 16;       // bytes per decoded row of values
+  static constexpr int LROW = KP * 4 + 16;       // bytes per decoded row of labels
+  static constexpr int VAL_BYTES = ROWS * VROW;
+  static constexpr int LAB_BYTES = ROWS * LROW;
+  static constexpr int STAGE_BYTES = (VAL_BYTES + LAB_BYTES + 127) / 128 * 128;
+  static constexpr int STAGE_OFF = NS * RAW_STAGE;
+  static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
+  static constexpr int LUT_BYTES = 2 * 256 * LREP * 4;
+  static constexpr int BAR_OFF = LUT_OFF + LUT_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + NS * 8 + 128;
+  static constexpr int WPR_ = BK / 4;            // raw words (4 codes) per operand row
+  static constexpr int UNITS = ROWS * WPR_;      // decode units: one raw word each
+  static constexpr int UPT = (UNITS + NT - 1) / NT;
+  static constexpr int NPIECE = NBLK - 1;
+  static_assert(G == 1 || G == 2 || G == 4, "lane groups of 1, 2 or 4");
+  static_assert(NPL >= 2 && NPL % 2 == 0, "whole 16-byte value chunks per lane and block");
+  static_assert(BM % WR == 0 && BN % WC == 0, "whole warps");
+  static_assert(NBLK >= 2, "the next stage's decode is dealt over the first NBLK - 1 blocks");
+  static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
+  static_assert(NT % WPR_ == 0, "a thread decodes the same word position of every row it takes");
+  static_assert(32 % LREP == 0, "table copies divide the warp");
+};
+
+constexpr int kClampE32 = 117 << 23;               // keep the scale positive (Inf/NaN c)
+
+template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB>
+__global__ void __launch_bounds__(BM * BN * G, MINB)
+emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
+                 const __grid_constant__ CUtensorMap tmB) {
+  using CS = ChainShape<BM, BN, G, BK, BLK, LREP>;
+  constexpr int NT = CS::NT, NPB = CS::NPB, NPL = CS::NPL, NBLK = CS::NBLK;
+  constexpr int NS = CS::NS, WPR_ = CS::WPR_;
+
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  unsigned char* const smem = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
+  uint32_t* lutA = reinterpret_cast<uint32_t*>(smem + CS::LUT_OFF);
+  uint32_t* lutB = lutA + 256 * LREP;
+  const uint32_t bar0 = smem_u32(smem + CS::BAR_OFF);
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int gl = lane % G;                              // lane within the group
+  const int gi = lane / G;                              // group within the warp
+  constexpr int WPR = BN / CS::WC;                      // warps along N
+  const int ty = (warp / WPR) * CS::WR + gi / CS::WC;   // output row in the CTA
+  const int tx = (warp % WPR) * CS::WC + gi % CS::WC;   // output column in the CTA
+  const int64_t m0 = ((int64_t)blockIdx.y + p.m_tile0) * BM;
+  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  const int s = blockIdx.z;
+
+  for (int i = tid; i < 256 * LREP; i += NT) {
+    lutA[i] = lut_entry((uint32_t)(i / LREP), p.fmt_a, kPreA);
+    lutB[i] = lut_entry((uint32_t)(i / LREP), p.fmt_b, kPreB);
+  }
+
+  // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
+  const int64_t K = p.K;
+  const int kt = p.S == 1 ? BK : p.ktile;
+  const int64_t T = (K + kt - 1) / kt;
+  int64_t t_begin, t_end, t_stride;
+  if (p.S == 1) { t_begin = 0; t_end = T; t_stride = 1; }
+  else if (p.scheme == 0) {
+    const int64_t q = (T + p.S - 1) / p.S;
+    t_begin = (int64_t)s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
+  } else { t_begin = s; t_end = T; t_stride = p.S; }
+  int64_t n_tiles = 0;
+  if (t_end > t_begin) n_tiles = (t_end - t_begin + t_stride - 1) / t_stride;
+  const int stages_per_tile = kt / BK;
+  int64_t n_stages = n_tiles * stages_per_tile;
+  if (n_tiles > 0) {
+    const int64_t t_last = t_begin + (n_tiles - 1) * t_stride;
+    const int64_t rem_last = K - t_last * kt;
+    const int64_t len_last = rem_last < kt ? rem_last : kt;
+    n_stages -= stages_per_tile - (len_last + BK - 1) / BK;
+  }
+  auto stage_k = [&](int64_t st) -> int {
+    const int64_t tl = st / stages_per_tile;
+    return (int)((t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK);
+  };
+  int64_t issued = 0;
+  auto issue = [&](int64_t st) {
+    issued = st + 1;
+    const int slot = (int)(st % NS);
+    const uint32_t bar = bar0 + 8u * slot;
+    const uint32_t dst = smem_u32(smem + slot * CS::RAW_STAGE);
+    const int k = stage_k(st);
+    mbar_arrive_expect_tx(bar, (uint32_t)(CS::RAW_A + CS::RAW_B));
+    tma_load_2d(dst, &tmA, k, (int)m0, bar);
+    tma_load_2d(dst + CS::RAW_A, &tmB, k, (int)n0, bar);
+  };
+  auto full_wait = [&](int64_t st) {
+    return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st % NS), (uint32_t)((st / NS) & 1), kWaitPolls);
+  };
+  auto give_up = [&](int64_t from) {
+    atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+    if (tid == 0)
+      for (int64_t x = from; x < issued; ++x) (void)full_wait(x);
+  };
+
+  // Decode.  Unit j of this thread is raw word dw of operand row dr0 + j * NT / WPR_
+  // (4 codes, two k-pairs): a warp reads consecutive words of a row and stores
+  // consecutive 16-byte value chunks and 8-byte label pairs.
+  const int dw = tid % WPR_, dr0 = tid / WPR_;
+  constexpr int DR_STEP = NT / WPR_;
+  const uint32_t* lutr = lutA + lane % LREP;            // this lane's copy of table A
+  auto decode_units = [&](int64_t st, int buf, int j0, int j1) {
+    const unsigned char* raw = smem + (int)(st % NS) * CS::RAW_STAGE + dr0 * BK + dw * 4;
+    unsigned char* vbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + dr0 * CS::VROW + dw * 16;
+    unsigned char* lbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + CS::VAL_BYTES +
+                           dr0 * CS::LROW + dw * 8;
+#pragma unroll
+    for (int j = j0; j < j1; ++j) {
+      const int r = dr0 + j * DR_STEP;
+      if (CS::UNITS % NT != 0 && r >= CS::ROWS) continue;
+      const uint32_t word = *reinterpret_cast<const uint32_t*>(raw + j * DR_STEP * BK);
+      const uint32_t* lut = lutr + (r < BM ? 0 : 256 * LREP);
+      uint32_t e[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) e[b] = lut[__byte_perm(word, 0u, 0x4440u | b) * LREP];
+      *reinterpret_cast<uint4*>(vbase + j * DR_STEP * CS::VROW) =
+          make_uint4(e[0] & 0xFFF00000u, e[1] & 0xFFF00000u, e[2] & 0xFFF00000u, e[3] & 0xFFF00000u);
+      *reinterpret_cast<uint2*>(lbase + j * DR_STEP * CS::LROW) =
+          make_uint2(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410));
+    }
+  };
+  auto decode_piece = [&](int64_t st, int buf, int piece) {
+    decode_units(st, buf, piece * CS::UPT / CS::NPIECE, (piece + 1) * CS::UPT / CS::NPIECE);
+  };
+
+  // Each lane reads its runs of a block from its own row bases.  One block step does
+  // the c-dependent work of block b (scale from max(E_p, e(c)), truncation, sum,
+  // normalise) and, interleaved with it in one instruction stream, the c-independent
+  // work of block b + 1: its exact products (packed k-pairs) and the group's label
+  // maximum (bits 23..30: e_a + e_b + 34; negative: no nonzero product).
+  const int lane_kp = gl * NPL;
+  const unsigned char* const vA0 = smem + CS::STAGE_OFF + ty * CS::VROW + lane_kp * 8;
+  const unsigned char* const vB0 = smem + CS::STAGE_OFF + (BM + tx) * CS::VROW + lane_kp * 8;
+  const unsigned char* const lA0 = smem + CS::STAGE_OFF + CS::VAL_BYTES + ty * CS::LROW + lane_kp * 4;
+  const unsigned char* const lB0 = smem + CS::STAGE_OFF + CS::VAL_BYTES + (BM + tx) * CS::LROW + lane_kp * 4;
+  auto load_labels = [&](int buf, int kb, uint32_t (&la)[NPL], uint32_t (&lb)[NPL]) {
+    const int off = buf * CS::STAGE_BYTES + kb * NPB * 4;
+    if constexpr (NPL % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < NPL / 4; ++i) {
+        const uint4 qa = *reinterpret_cast<const uint4*>(lA0 + off + i * 16);
+        const uint4 qb = *reinterpret_cast<const uint4*>(lB0 + off + i * 16);
+        la[4 * i] = qa.x; la[4 * i + 1] = qa.y; la[4 * i + 2] = qa.z; la[4 * i + 3] = qa.w;
+        lb[4 * i] = qb.x; lb[4 * i + 1] = qb.y; lb[4 * i + 2] = qb.z; lb[4 * i + 3] = qb.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NPL / 2; ++i) {
+        const uint2 qa = *reinterpret_cast<const uint2*>(lA0 + off + i * 8);
+        const uint2 qb = *reinterpret_cast<const uint2*>(lB0 + off + i * 8);
+        la[2 * i] = qa.x; la[2 * i + 1] = qa.y; lb[2 * i] = qb.x; lb[2 * i + 1] = qb.y;
+      }
+    }
+  };
+  auto load_values = [&](int buf, int kb, f32x2_t (&va)[NPL], f32x2_t (&vb)[NPL]) {
+    const int off = buf * CS::STAGE_BYTES + kb * NPB * 8;
+#pragma unroll
+    for (int i = 0; i < NPL / 2; ++i) {
+      const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(vA0 + off + i * 16);
+      const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(vB0 + off + i * 16);
+      va[2 * i] = qa.x; va[2 * i + 1] = qa.y;
+      vb[2 * i] = qb.x; vb[2 * i + 1] = qb.y;
+    }
+  };
+  // the group's maximum of the pass-1 accumulators, both halves, high half kept
+  auto finish_ep = [&](uint32_t e0, uint32_t e1) -> int {
+    uint32_t e = __vmaxs2(e0, e1);
+    e = __vmaxs2(e, __byte_perm(e, 0u, 0x1032));       // even and odd k: both halves
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) e = __vmaxs2(e, __shfl_xor_sync(0xFFFFFFFFu, e, off));
+    return (int)(e & 0xFFFF0000u);
+  };
+  // block 0's c-independent work alone (no c-dependent step to interleave with)
+  auto prefetch = [&](int buf, int kb, f32x2_t (&x2)[NPL], int& ep32) {
+    uint32_t la[NPL], lb[NPL];
+    f32x2_t va[NPL], vb[NPL];
+    load_labels(buf, kb, la, lb);
+    load_values(buf, kb, va, vb);
+    uint32_t e0 = 0x80008000u, e1 = 0x80008000u;
+#pragma unroll
+    for (int q = 0; q < NPL; ++q) {
+      x2[q] = fmul2_rn(va[q], vb[q]);
+      if (q & 1) e1 = __viaddmax_s16x2(la[q], lb[q], e1);
+      else e0 = __viaddmax_s16x2(la[q], lb[q], e0);
+    }
+    ep32 = finish_ep(e0, e1);
+  };
+
+  float c = 0.0f;        // chain state c' = c * 2^-93
+  float accs = 0.0f;     // slow: K-order fp32 sum of the chunk results
+  int bic = 0;           // slow: blocks in the current chunk
+  // one block step: the c-dependent work of the block in (xc, epc) and, when next,
+  // the c-independent work of block kb of buffer buf into (xc, epc) for the next step
+  auto step = [&](f32x2_t (&xc)[NPL], int& epc, bool next, int buf, int kb) {
+    uint32_t la[NPL], lb[NPL];
+    f32x2_t va[NPL], vb[NPL];
+    if (next) {
+      load_labels(buf, kb, la, lb);
+      load_values(buf, kb, va, vb);
+    }
+    int E = max(epc, (int)(__float_as_uint(c) & 0x7F800000u));
+    E = min(E, kClampE32);
+    const uint32_t sc = kScaleBase - (uint32_t)E;
+    const float scf = __uint_as_float(sc);
+    const f32x2_t sc2 = pack2(scf, scf);
+    f32x2_t s0 = pack2((G == 1 || gl == 0) ? fmul_rz(c, scf) : 0.0f, 0.0f);
+    f32x2_t s1 = pack2(0.0f, 0.0f);
+    uint32_t e0 = 0x80008000u, e1 = 0x80008000u;
+#pragma unroll
+    for (int q = 0; q < NPL; ++q) {
+      const f32x2_t t = fmul2_rz(xc[q], sc2);
+      if (q & 1) s1 = fadd2_rn(s1, t);
+      else s0 = fadd2_rn(s0, t);
+      if (next) {
+        xc[q] = fmul2_rn(va[q], vb[q]);
+        if (q & 1) e1 = __viaddmax_s16x2(la[q], lb[q], e1);
+        else e0 = __viaddmax_s16x2(la[q], lb[q], e0);
+      }
+    }
+    float sum = sum_halves(fadd2_rn(s0, s1));
+    if (next) epc = finish_ep(e0, e1);
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) sum = fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, off));
+    c = __uint_as_float(__float_as_uint(fmul_rn(sum, __uint_as_float(kInvBase - sc))) & kKeep14);
+    if (SLOW) {
+      if (++bic == p.restart_blocks) {
+        accs = fadd_rn(accs, fmul_rn(c, kTwo93));
+        c = 0.0f;
+        bic = 0;
+      }
+    }
+  };
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8u * i, 1u);
+    fence_mbar_init();
+  }
+  __syncthreads();                       // tables and barriers ready
+  if (tid == 0)
+    for (int64_t st = 0; st < NS && st < n_stages; ++st) issue(st);
+
+  bool timed_out = false;
+  if (n_stages > 0) {
+    timed_out = !full_wait(0);
+    if (!timed_out) decode_units(0, 0, 0, CS::UPT);
+  }
+  if (__syncthreads_or(timed_out)) { give_up(0); return; }
+  if (tid == 0 && NS < n_stages) {
+    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
+    issue(NS);
+  }
+  f32x2_t xc[NPL];
+  int epc = 0;
+  if (n_stages > 0) prefetch(0, 0, xc, epc);
+  // every stage but the last: the next stage's decode is dealt over the first NBLK - 1
+  // block steps (a wait that gave up leaves garbage there; the barrier then ends the CTA)
+  for (int64_t st = 0; st + 1 < n_stages; ++st) {
+    const int cur = (int)(st & 1), nxt = cur ^ 1;
+    timed_out = !full_wait(st + 1);
+#pragma unroll
+    for (int bb = 0; bb + 1 < NBLK; ++bb) {
+      step(xc, epc, true, cur, bb + 1);
+      decode_piece(st + 1, nxt, bb);
+    }
+    // the next stage is decoded: everyone may read it, and its raw slot is free
+    if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
+    if (tid == 0 && st + 1 + NS < n_stages) {
+      fence_proxy_async();
+      issue(st + 1 + NS);
+    }
+    step(xc, epc, true, nxt, 0);
+  }
+  if (n_stages > 0) {                    // the last stage
+    const int cur = (int)((n_stages - 1) & 1);
+#pragma unroll
+    for (int bb = 0; bb + 1 < NBLK; ++bb) step(xc, epc, true, cur, bb + 1);
+    step(xc, epc, false, cur, 0);
+  }
+
+  float res;
+  if (SLOW) res = bic ? fadd_rn(accs, fmul_rn(c, kTwo93)) : accs;
+  else res = fmul_rn(c, kTwo93);
+  if (G > 1 && gl != 0) return;             // the group's lanes hold the same result
+  const int64_t m = m0 + ty, n = n0 + tx;
+  if (m >= p.M || n >= p.N) return;
+  if (p.S > 1) {
+    p.partial[(int64_t)s * p.M * p.N + m * p.N + n] = res;
+    return;
+  }
+  const float alpha = fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b));
+  const OutStore store(p);
+  store(p, m * p.N + n, fma_plus0(res, alpha));
 }
 
 // ---------------------------------------------------------------------------

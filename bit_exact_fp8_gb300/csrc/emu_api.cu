@@ -52,49 +52,47 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 //        (K8/K4: shapes with few, long chains, e.g. small M x N with split-K, where a
 //        CTA tile must stay tiny for every SM to get work; one or two products per
 //        lane and block, so they keep scalar FP32)
+//   C2, C4, C1, C1L: chain tiles (emu_chain_kernel), one output per group of 2, 4,
+//        1, 1 lanes, 8 x 8, 8 x 4, 8 x 8 and 16 x 16 outputs per CTA: the next block's
+//        products and label maximum computed inside the current block's c-dependent
+//        step (skinny split-K shapes and M of about 8 to 12)
 struct TileInfo {
   const char* name;
   int tm, tn, bm, bn, threads;
   int resident, resident_slow;  // CTAs per SM (shared memory and the register budget)
   int bk, g;                    // chain tiles: bk of 32-product blocks (16-product: 64)
-  // cost model, both fitted to GB300 measurements (SM clocks per K element) on the
-  // benchmark workloads and on M = 1 .. 512 at N = 5760, K = 1920:
+  // cost model, fitted to GB300 measurements on the benchmark workloads and on M = 1
+  // .. 512 at N = 5760, K = 1920 (SM clocks per K element of a chain, and per wave):
   double ipm;                   // effective thread instructions per MAC at full load
-  double lat;                   // one CTA alone on an SM
+  double lat;                   // one CTA alone on an SM (32-product blocks)
+  double lat16;                 // the same with 16-product blocks
+  double fixed;                 // per wave of resident CTAs, independent of K
   double slow_factor;           // slow accumulation's extra cost
   bool one_wave;                // a candidate only if its CTAs fit in one wave
 };
 // resident is also the kernel's __launch_bounds__ minimum, which holds ptxas to
 // 65536 / (resident * threads) registers
 constexpr TileInfo kTiles[] = {
-    {"M40", 4, 2, 64, 40, 320, 1, 1, 128, 1, 6.2, 131.0, 1.0, false},
-    {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 6.0, 200.0, 1.0, false},
-    {"S", 2, 2, 16, 16, 64, 6, 6, 64, 1, 11.5, 49.0, 1.0, false},
-    {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 38.0, 36.0, 1.0, false},
-    {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 33.0, 33.0, 1.0, false},
-    {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 1.08, false},
-    {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 35.0, 18.0, 1.0, true},
-    {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 26.0, 21.0, 1.0, true},
-    // chain tiles (emu_chain_kernel): one output per lane group of g lanes
-    {"C2", 1, 1, 8, 8, 128, 2, 2, 128, 2, 1e9, 1e9, 1.0, false},
-    {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 1e9, 1e9, 1.0, false},
-    {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 1e9, 1e9, 1.0, false},
-    {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 1e9, 1e9, 1.0, false},
-    // large tiles with two blocks per 64-code stage (the second block's pass 1 runs
-    // inside the first block's pass 2), one CTA per SM
-    {"M64K", 4, 4, 64, 64, 256, 1, 1, 64, 1, 1e9, 1e9, 1.0, false},
-    {"M128", 4, 4, 128, 64, 512, 1, 1, 64, 1, 1e9, 1e9, 1.0, false},
-    // M64 and M32 with the labels of the next stage decoded a stage ahead
-    {"M64A", 4, 4, 64, 64, 256, 2, 1, 32, 1, 1e9, 1e9, 1.0, false},
-    {"M32A", 4, 4, 64, 32, 128, 3, 3, 32, 1, 1e9, 1e9, 1.0, false},
+    {"M40", 4, 2, 64, 40, 320, 1, 1, 128, 1, 6.2, 131.0, 131.0, 0.0, 1.0, false},
+    {"M32", 4, 4, 64, 32, 128, 3, 3, 32, 1, 6.0, 200.0, 200.0, 0.0, 1.0, false},
+    {"S", 2, 2, 16, 16, 64, 6, 6, 64, 1, 11.5, 49.0, 49.0, 0.0, 1.0, false},
+    {"K8", 1, 2, 4, 8, 128, 8, 8, 64, 8, 38.0, 36.0, 36.0, 0.0, 1.0, false},
+    {"K4", 1, 2, 4, 16, 128, 8, 8, 64, 4, 33.0, 33.0, 33.0, 0.0, 1.0, false},
+    {"M64", 4, 4, 64, 64, 256, 2, 1, 32, 1, 5.2, 200.0, 200.0, 0.0, 1.08, false},
+    {"K8H", 1, 2, 4, 8, 128, 7, 7, 128, 8, 35.0, 18.0, 18.0, 0.0, 1.0, true},
+    {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 26.0, 21.0, 21.0, 0.0, 1.0, true},
+    // chain tiles (emu_chain_kernel): one output per lane group of g lanes; 128-code
+    // stages for 32-product blocks, 64-code stages for 16-product blocks
+    {"C2", 1, 1, 8, 8, 128, 2, 2, 128, 2, 17.5, 12.0, 18.0, 13000.0, 1.0, false},
+    {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 53.0, 13.3, 20.6, 13000.0, 1.0, false},
+    {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 17.5, 14.0, 17.0, 10000.0, 1.0, false},
+    {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 12.5, 26.0, 26.5, 12000.0, 1.0, false},
 };
-constexpr int kNumTiles = 16;
+constexpr int kNumTiles = 12;
 constexpr int kFirstChainTile = 8;
 // K-stage of a tile for blocks of blk products (the chain tiles stage 64 codes for
 // 16-product blocks)
-int tile_bk(int t, int blk) {
-  return (t >= kFirstChainTile && t < kFirstChainTile + 4 && blk == 16) ? 64 : kTiles[t].bk;
-}
+int tile_bk(int t, int blk) { return (t >= kFirstChainTile && blk == 16) ? 64 : kTiles[t].bk; }
 // SMs of the current device (152 on a GB300), cached per device (atomics: the entry
 // points may be called from several host threads)
 int sm_count() {
@@ -153,13 +151,13 @@ int make_operand_map(CUtensorMap* map, const uint8_t* base, int64_t rows, int64_
 }
 
 template <int TM, int TN, int WM, int WN, int BK, int BLK, bool SLOW, int G, int MINB, bool PK,
-          bool LA = false, int LREP = 1>
+          int LREP = 1>
 int launch_one(const emu::GemmParams& p, cudaStream_t st) {
   using TS = emu::TileShape<TM, TN, WM, WN, BK, G, LREP>;
   // the resident CTAs the register budget is set for also fit in shared memory
   // (228 KB per SM, 1 KB of it reserved per CTA)
   static_assert(MINB * (TS::SMEM_BYTES + 1024) <= 228 * 1024, "resident CTAs fit in shared memory");
-  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK, LA, LREP>;
+  auto kern = emu::emu_gemm_kernel<TM, TN, WM, WN, BK, BLK, SLOW, G, MINB, PK, LREP>;
   // the dynamic shared memory limit is a per-function, per-device attribute; setting
   // it twice (two host threads racing on the first call) is harmless
   static std::atomic<bool> configured[64];
@@ -190,15 +188,14 @@ int launch_one(const emu::GemmParams& p, cudaStream_t st) {
 // MINB, MINB_SLOW: the CTAs per SM the fast and slow variants are meant to keep
 // resident (the register budget ptxas is held to)
 template <int TM, int TN, int WM, int WN, int BK, int G, int MINB, int MINB_SLOW = MINB,
-          bool PK = true, bool LA = false, int LREP = 1>
+          bool PK = true, int LREP = 1>
 int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, G, MINB_SLOW, PK, LA, LREP>(p, st)
-                : launch_one<TM, TN, WM, WN, BK, 32, false, G, MINB, PK, LA, LREP>(p, st);
+    return slow ? launch_one<TM, TN, WM, WN, BK, 32, true, G, MINB_SLOW, PK, LREP>(p, st)
+                : launch_one<TM, TN, WM, WN, BK, 32, false, G, MINB, PK, LREP>(p, st);
   }
-  // 16-product blocks take the tile without labels ahead (it needs one block per stage)
-  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, G, MINB_SLOW, PK, false, LREP>(p, st)
-              : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK, false, LREP>(p, st);
+  return slow ? launch_one<TM, TN, WM, WN, BK, 16, true, G, MINB_SLOW, PK, LREP>(p, st)
+              : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK, LREP>(p, st);
 }
 
 template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB>
@@ -240,9 +237,10 @@ int launch_chain(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) 
               : launch_chain_one<BM, BN, G, 64, 16, false, LREP, MINB>(p, st);
 }
 
-// Pick the tile with the lowest estimated time per K element, in SM clocks: the
-// larger of the issue time of the CTAs an SM receives and the latency-bound time of
-// its waves of resident CTAs.  EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
+// Pick the tile with the lowest estimated time in SM clocks: per K element of a
+// chain, the larger of the issue time of the CTAs an SM receives and the latency of
+// its waves of resident CTAs; times the chain's length; plus a fixed cost per wave.
+// EMU_FP8_TILE=<name> forces a tile (for tuning sweeps).
 int choose_tile(const emu::GemmParams& p, int blk, bool slow, double sms) {
   static const int forced = [] {         // read once (thread-safe static initialisation)
     const char* env = getenv("EMU_FP8_TILE");
@@ -256,6 +254,7 @@ int choose_tile(const emu::GemmParams& p, int blk, bool slow, double sms) {
   auto ctas_of = [&](const TileInfo& ti) {
     return (double)((p.N + ti.bn - 1) / ti.bn) * (double)((p.M + ti.bm - 1) / ti.bm) * p.S;
   };
+  const double chain_k = (double)p.K / p.S;
   int best = -1;
   double best_cost = 0.0;
   for (int t = 0; t < kNumTiles; ++t) {
@@ -264,21 +263,19 @@ int choose_tile(const emu::GemmParams& p, int blk, bool slow, double sms) {
     const int resident = slow ? ti.resident_slow : ti.resident;
     const double per_sm = std::ceil(ctas_of(ti) / sms);
     if (ti.one_wave && per_sm > resident) continue;
+    const double waves = std::ceil(per_sm / resident);
     const double t_issue = per_sm * ti.bm * ti.bn * ti.ipm / 128.0;
-    const double t_latency = std::ceil(per_sm / resident) * ti.lat;
-    const double est = std::max(t_issue, t_latency) * (slow ? ti.slow_factor : 1.0);
+    const double t_latency = waves * (blk == 16 ? ti.lat16 : ti.lat);
+    const double est = (std::max(t_issue, t_latency) * chain_k + waves * ti.fixed) *
+                       (slow ? ti.slow_factor : 1.0);
     if (best < 0 || est < best_cost) { best = t; best_cost = est; }
   }
   return best;
 }
 
-// decode-table copies per tile (the lanes sharing a copy, 32 / LREP, contend for its banks);
-// the residency each tile is built for bounds them through its shared memory
-#ifndef EMU_LREP
-#define EMU_LREP 8
-#endif
-constexpr int LREP_M40 = EMU_LREP, LREP_M32 = EMU_LREP, LREP_M64 = EMU_LREP, LREP_S = 2,
-              LREP_K = 2;
+// decode-table copies per tile (the lanes sharing a copy, 32 / LREP, contend for its
+// banks); the residency each tile is built for bounds them through its shared memory
+constexpr int LREP_M40 = 8, LREP_M32 = 8, LREP_M64 = 8, LREP_S = 2, LREP_K = 2;
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   switch (choose_tile(p, blk, slow, sm_count())) {
@@ -286,18 +283,14 @@ int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
     case 9: return launch_chain<8, 4, 4, 32, 2>(p, blk, slow, st);
     case 10: return launch_chain<8, 8, 1, 8, 4>(p, blk, slow, st);
     case 11: return launch_chain<16, 16, 1, 8, 2>(p, blk, slow, st);
-    case 12: return launch_tile<4, 4, 16, 16, 64, 1, 1, 1, true, false, 8>(p, blk, slow, st);
-    case 13: return launch_tile<4, 4, 32, 16, 64, 1, 1, 1, true, false, 8>(p, blk, slow, st);
-    case 14: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1, true, true, LREP_M64>(p, blk, slow, st);
-    default: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, true, LREP_M32>(p, blk, slow, st);
-    case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1, 1, true, false, LREP_M40>(p, blk, slow, st);
-    case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, false, LREP_M32>(p, blk, slow, st);
-    case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6, 6, true, false, LREP_S>(p, blk, slow, st);
-    case 3: return launch_tile<1, 2, 4, 4, 64, 8, 8, 8, false, false, LREP_K>(p, blk, slow, st);
-    case 4: return launch_tile<1, 2, 4, 8, 64, 4, 8, 8, false, false, LREP_K>(p, blk, slow, st);
-    case 5: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1, true, false, LREP_M64>(p, blk, slow, st);
-    case 6: return launch_tile<1, 2, 4, 4, 128, 8, 7, 7, false, false, LREP_K>(p, blk, slow, st);
-    case 7: return launch_tile<1, 2, 4, 8, 128, 4, 4, 4, false, false, LREP_K>(p, blk, slow, st);
+    case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1, 1, true, LREP_M40>(p, blk, slow, st);
+    case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, LREP_M32>(p, blk, slow, st);
+    case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6, 6, true, LREP_S>(p, blk, slow, st);
+    case 3: return launch_tile<1, 2, 4, 4, 64, 8, 8, 8, false, LREP_K>(p, blk, slow, st);
+    case 4: return launch_tile<1, 2, 4, 8, 64, 4, 8, 8, false, LREP_K>(p, blk, slow, st);
+    case 5: return launch_tile<4, 4, 16, 16, 32, 1, 2, 1, true, LREP_M64>(p, blk, slow, st);
+    case 6: return launch_tile<1, 2, 4, 4, 128, 8, 7, 7, false, LREP_K>(p, blk, slow, st);
+    default: return launch_tile<1, 2, 4, 8, 128, 4, 4, 4, false, LREP_K>(p, blk, slow, st);
   }
 }
 

@@ -257,6 +257,27 @@ __device__ __forceinline__ uint32_t lut_entry(uint32_t code, int fmt, int pre) {
   return (__float_as_uint(v) & 0xFFF00000u) | ((uint32_t)lab & 0xFFFFu);
 }
 
+// Fill both operands' replicated decode tables (lut: 512 * LREP words, A's codes
+// then B's): each of the 512 entries is decoded once into staging (2 KB of shared
+// memory not otherwise in use yet), then broadcast to its LREP copies with 16-byte
+// stores.  Ends with a barrier.
+template <int LREP, int NT>
+__device__ __forceinline__ void fill_luts(uint32_t* lut, uint32_t* staging, int fmt_a, int fmt_b,
+                                          int tid) {
+  for (int c = tid; c < 512; c += NT)
+    staging[c] = c < 256 ? lut_entry((uint32_t)c, fmt_a, kPreA) : lut_entry((uint32_t)(c - 256), fmt_b, kPreB);
+  __syncthreads();
+  if constexpr (LREP % 4 == 0) {
+    for (int i = tid; i < 512 * LREP / 4; i += NT) {
+      const uint32_t e = staging[i / (LREP / 4)];
+      reinterpret_cast<uint4*>(lut)[i] = make_uint4(e, e, e, e);
+    }
+  } else {
+    for (int i = tid; i < 512 * LREP; i += NT) lut[i] = staging[i / LREP];
+  }
+  __syncthreads();
+}
+
 // N consecutive 32-bit words from shared memory, p aligned to 4 * (N & -N) bytes,
 // in the widest loads that alignment allows
 template <int N>
@@ -334,10 +355,11 @@ struct TileShape {
   // dynamic shared memory to request: the layout plus room to align its base
   static constexpr int SMEM_BYTES = BAR_OFF + NS * 8 + RAW_ALIGN;
   static_assert(RAW_A % RAW_ALIGN == 0, "the B box of a slot starts aligned");
+  static_assert(NS * RAW_STAGE >= 2048, "the raw ring stages the decode-table entries");
 };
 
 template <int TM, int TN, int WM, int WN, int BK_, int BLK, bool SLOW, int G, int MINB,
-          bool PK, bool LA = false, int LREP = 1>
+          bool PK, int LREP = 1>
 __global__ void __launch_bounds__(WM * WN * G, MINB)
 emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB) {
@@ -383,45 +405,41 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int64_t m0 = ((int64_t)blockIdx.y + p.m_tile0) * BM;
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int s = blockIdx.z;
+  // decode tables: code -> (pre-scaled value bits, label) for each operand (the raw
+  // ring, still unused, stages the entries)
+  fill_luts<LREP, NT>(lutA, reinterpret_cast<uint32_t*>(smem), p.fmt_a, p.fmt_b, tid);
 
-  // decode tables: code -> (pre-scaled value bits, label) for each operand
-  for (int i = tid; i < 256 * LREP; i += NT) {
-    lutA[i] = lut_entry((uint32_t)(i / LREP), p.fmt_a, kPreA);
-    lutB[i] = lut_entry((uint32_t)(i / LREP), p.fmt_b, kPreB);
-  }
-
-  // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
-  const int64_t K = p.K;
+  // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end); stage st
+  // is sub-stage st % spt of the chain's tile st / spt (K < 2^31: 32-bit counts)
+  const int K = (int)p.K;
   const int kt = p.S == 1 ? BK : p.ktile;    // unsplit: any tiling of K is the same chain
-  const int64_t T = (K + kt - 1) / kt;
-  int64_t t_begin, t_end, t_stride;
+  const int T = (K + kt - 1) / kt;
+  int t_begin, t_end, t_stride;
   if (p.S == 1) { t_begin = 0; t_end = T; t_stride = 1; }
   else if (p.scheme == 0) {
-    const int64_t q = (T + p.S - 1) / p.S;
-    t_begin = (int64_t)s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
+    const int q = (T + p.S - 1) / p.S;
+    t_begin = s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
   } else { t_begin = s; t_end = T; t_stride = p.S; }
-  int64_t n_tiles = 0;
-  if (t_end > t_begin) n_tiles = (t_end - t_begin + t_stride - 1) / t_stride;
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + t_stride - 1) / t_stride : 0;
   const int stages_per_tile = kt / BK;
-  int64_t n_stages = n_tiles * stages_per_tile;
+  int n_stages = n_tiles * stages_per_tile;
   // the last tile of the chain may be short (only tile T-1 can be)
   if (n_tiles > 0) {
-    const int64_t t_last = t_begin + (n_tiles - 1) * t_stride;
-    const int64_t rem_last = K - t_last * kt;
-    const int64_t len_last = rem_last < kt ? rem_last : kt;
+    const int t_last = t_begin + (n_tiles - 1) * t_stride;
+    const int len_last = K - t_last * kt < kt ? K - t_last * kt : kt;
     n_stages -= stages_per_tile - (len_last + BK - 1) / BK;
   }
 
-  auto stage_k = [&](int64_t st) -> int {
-    const int64_t tl = st / stages_per_tile;
-    return (int)((t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK);
+  auto stage_k = [&](int st) -> int {
+    if (stages_per_tile == 1) return (t_begin + st * t_stride) * kt;
+    return (t_begin + (st / stages_per_tile) * t_stride) * kt + (st % stages_per_tile) * BK;
   };
   // one thread: start the TMA loads of stage st into its ring slot.  Boxes reaching
   // past M, N or K are zero-filled, and zero codes are neutral in every block.
-  int64_t issued = 0;                        // stages whose loads thread 0 started
-  auto issue = [&](int64_t st) {
+  int issued = 0;                            // stages whose loads thread 0 started
+  auto issue = [&](int st) {
     issued = st + 1;
-    const int slot = (int)(st % NS);
+    const int slot = st % NS;
     const uint32_t bar = bar0 + 8u * slot;
     const uint32_t dst = smem_u32(smem + slot * TS::RAW_STAGE);
     const int k = stage_k(st);
@@ -429,10 +447,9 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     tma_load_2d(dst, &tmA, k, (int)m0, bar);
     tma_load_2d(dst + TS::RAW_A, &tmB, k, (int)n0, bar);
   };
-  // the decoder threads: decode the raw slot of stage st into operand buffer buf;
-  // what: 1 values, 2 labels, 3 both
-  auto decode_stage = [&](int64_t st, int buf, int what) {
-    const unsigned char* raw = smem + (int)(st % NS) * TS::RAW_STAGE;
+  // the decoder threads: decode the raw slot of stage st into operand buffer buf
+  auto decode_stage = [&](int st, int buf) {
+    const unsigned char* raw = smem + (st % NS) * TS::RAW_STAGE;
     unsigned char* base = smem + TS::STAGE_OFF + buf * TS::STAGE_BYTES;
     float* sAv = reinterpret_cast<float*>(base + TS::A_VAL);
     uint32_t* sAl = reinterpret_cast<uint32_t*>(base + TS::A_LAB);   // label pairs
@@ -466,15 +483,13 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           const uint32_t e1 = lA[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3)) * LREP];
           const uint2 d0 = make_uint2(e0 & 0xFFF00000u, 0u), d1 = make_uint2(e1 & 0xFFF00000u, 0u);
           const uint32_t lp = __byte_perm(e0, e1, 0x5410);
-          if (what & 1) {
-            if (PK) {
-              *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = make_uint2(d0.x, d1.x);
-            } else {
-              sAv[(h * 16 + j) * BM + h * PAD + row] = __uint_as_float(d0.x);
-              sAv[(h * 16 + j + 1) * BM + h * PAD + row] = __uint_as_float(d1.x);
-            }
+          if (PK) {
+            *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = make_uint2(d0.x, d1.x);
+          } else {
+            sAv[(h * 16 + j) * BM + h * PAD + row] = __uint_as_float(d0.x);
+            sAv[(h * 16 + j + 1) * BM + h * PAD + row] = __uint_as_float(d1.x);
           }
-          if (what & 2) sAl[(h * 8 + j / 2) * BM + h * PAD + row] = lp;
+          sAl[(h * 8 + j / 2) * BM + h * PAD + row] = lp;
         }
       } else if (c < A_CHUNKS + B_CHUNKS) {
         const int cb = c - A_CHUNKS;
@@ -488,16 +503,14 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           const uint32_t e1 = lB[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3)) * LREP];
           const uint2 d0 = make_uint2(e0 & 0xFFF00000u, 0u), d1 = make_uint2(e1 & 0xFFF00000u, 0u);
           const uint32_t lp = __byte_perm(e0, e1, 0x5410);
-          if (what & 1) {
-            if (PK) {
-              *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
-                  make_uint2(d0.x, d1.x);
-            } else {
-              sBv[(h * 16 + j) * BN + h * PAD + col] = __uint_as_float(d0.x);
-              sBv[(h * 16 + j + 1) * BN + h * PAD + col] = __uint_as_float(d1.x);
-            }
+          if (PK) {
+            *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(col)) * 2) =
+                make_uint2(d0.x, d1.x);
+          } else {
+            sBv[(h * 16 + j) * BN + h * PAD + col] = __uint_as_float(d0.x);
+            sBv[(h * 16 + j + 1) * BN + h * PAD + col] = __uint_as_float(d1.x);
           }
-          if (what & 2) sBl[(h * 8 + j / 2) * BN + h * PAD + col] = lp;
+          sBl[(h * 8 + j / 2) * BN + h * PAD + col] = lp;
         }
       }
     }
@@ -516,17 +529,19 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     fence_mbar_init();
   }
   __syncthreads();                       // tables and barriers ready
-  if (tid == 0)
-    for (int64_t st = 0; st < NS && st < n_stages; ++st) issue(st);
-  auto full_wait = [&](int64_t st) {
+  if (tid == 0) {
+    fence_proxy_async();                 // the ring staged the tables (generic stores)
+    for (int st = 0; st < NS && st < n_stages; ++st) issue(st);
+  }
+  auto full_wait = [&](int st) {
     return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st % NS), (uint32_t)((st / NS) & 1), kWaitPolls);
   };
   // after a wait gave up: record it; thread 0 waits (bounded) for its loads still in
   // flight from stage `from` on, so that none lands after the CTA has exited
-  auto give_up = [&](int64_t from) {
+  auto give_up = [&](int from) {
     atomicExch(&g_emu_device_status, kStatusWaitTimeout);
     if (tid == 0)
-      for (int64_t x = from; x < issued; ++x) (void)full_wait(x);
+      for (int x = from; x < issued; ++x) (void)full_wait(x);
   };
 
   // ---- the chain: per block, pass 1 (block maximum of the label sums), scales,
@@ -556,11 +571,7 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // block's pass 1 (DPX, integer pipe) inside this block's pass-2 loop (FP32 pipe),
   // so one instruction stream feeds both pipes; the stage's first block runs its
   // own pass 1.
-  // LA (labels one stage ahead, tiles with one block per stage): the labels of stage
-  // st + 1 are decoded during stage st - 1, so every block's pass 1 runs inside the
-  // previous block's pass 2, across the stage boundary
-  static_assert(!LA || (NBLK == 1 && PK && G == 1), "labels ahead: one packed block per stage");
-  constexpr bool kFuse = PK && G == 1 && ((!SLOW && NBLK >= 2) || LA);
+  constexpr bool kFuse = PK && G == 1 && !SLOW && NBLK >= 2;
   uint32_t En[TM][TN];   // the next block's maxima while fused
   // one block of every chain, from the decoded buffer at `base`
   auto block_step = [&](const unsigned char* base, int k0, bool have_e2, bool fuse_next,
@@ -702,72 +713,33 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   };
 
   bool timed_out = false;
-  if constexpr (LA) {
-    // stage st computes its block from values[st & 1] with the next block's pass 1 on
-    // labels[(st + 1) & 1], decodes the values of st + 1 and the labels of st + 2, then
-    // one barrier; the raw slot of st + 1 is then fully decoded and refilled
-    if (n_stages > 0) {
-      timed_out = !full_wait(0);
-      if (!timed_out) decode_stage(0, 0, 3);
-      if (n_stages > 1 && !timed_out) {
-        timed_out = !full_wait(1);
-        if (!timed_out) decode_stage(1, 1, 2);
-      }
-    }
-    if (__syncthreads_or(timed_out)) { give_up(0); return; }
-    if (tid == 0 && NS < n_stages) {
-      fence_proxy_async();
-      issue(NS);
-    }
-    if (n_stages > 0) {
-      pass1_reset();
-#pragma unroll
-      for (int q = 0; q < BLK / 2; ++q) pass1_pair_into(E2, smem + TS::STAGE_OFF, 0, q);
-    }
-    for (int64_t st = 0; st < n_stages; ++st) {
-      const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
-      const unsigned char* nxt = smem + TS::STAGE_OFF + (int)((st + 1) & 1) * TS::STAGE_BYTES;
-      block_step(cur, 0, true, st + 1 < n_stages, nxt, 0);
-      if (st + 1 < n_stages) decode_stage(st + 1, (int)((st + 1) & 1), 1);
-      if (st + 2 < n_stages) {
-        timed_out = !full_wait(st + 2);
-        if (!timed_out) decode_stage(st + 2, (int)(st & 1), 2);
-      }
-      if (__syncthreads_or(timed_out)) { give_up(st + 2); return; }
-      if (tid == 0 && st + 1 + NS < n_stages) {
-        fence_proxy_async();
-        issue(st + 1 + NS);
-      }
-    }
-  } else {
-    // decode stage st + 1 into the other buffer while nobody reads it, then one
-    // barrier per stage; thread 0 refills the ring slot everyone has decoded
-    if (n_stages > 0) {
-      timed_out = !full_wait(0);
-      decode_stage(0, 0, 3);
-    }
-    if (__syncthreads_or(timed_out)) { give_up(0); return; }
-    if (tid == 0 && NS < n_stages) {
-      fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
-      issue(NS);
-    }
-    for (int64_t st = 0; st < n_stages; ++st) {
-      const unsigned char* cur = smem + TS::STAGE_OFF + (int)(st & 1) * TS::STAGE_BYTES;
-      // slow chains of the large tiles: the blocks of a stage stay a loop (a restart
-      // may fall after any of them; unrolled, the 64 x 40 tile's 32-product variant
-      // spilled registers); the small tiles unroll them
+  // decode stage st + 1 into the other buffer while nobody reads it, then one
+  // barrier per stage; thread 0 refills the ring slot everyone has decoded
+  if (n_stages > 0) {
+    timed_out = !full_wait(0);
+    decode_stage(0, 0);
+  }
+  if (__syncthreads_or(timed_out)) { give_up(0); return; }
+  if (tid == 0 && NS < n_stages) {
+    fence_proxy_async();                 // the slot's reads (before the barrier) precede its refill
+    issue(NS);
+  }
+  for (int st = 0; st < n_stages; ++st) {
+    const unsigned char* cur = smem + TS::STAGE_OFF + (st & 1) * TS::STAGE_BYTES;
+    // slow chains of the large tiles: the blocks of a stage stay a loop (a restart
+    // may fall after any of them; unrolled, the 64 x 40 tile's 32-product variant
+    // spilled registers); the small tiles unroll them
 #pragma unroll (SLOW && BM * BN > 1024 ? 1 : NBLK)
-      for (int bb = 0; bb < NBLK; ++bb)
-        block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK, cur, bb * BLK + BLK);
-      if (st + 1 < n_stages) {
-        timed_out = !full_wait(st + 1);
-        decode_stage(st + 1, (int)((st + 1) & 1), 3);
-      }
-      if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
-      if (tid == 0 && st + 1 + NS < n_stages) {
-        fence_proxy_async();
-        issue(st + 1 + NS);
-      }
+    for (int bb = 0; bb < NBLK; ++bb)
+      block_step(cur, bb * BLK, kFuse && bb > 0, kFuse && bb + 1 < NBLK, cur, bb * BLK + BLK);
+    if (st + 1 < n_stages) {
+      timed_out = !full_wait(st + 1);
+      decode_stage(st + 1, (st + 1) & 1);
+    }
+    if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
+    if (tid == 0 && st + 1 + NS < n_stages) {
+      fence_proxy_async();
+      issue(st + 1 + NS);
     }
   }
 
@@ -839,10 +811,9 @@ struct ChainShape {
   static constexpr int NBLK = BK / BLK;
   static constexpr int RAW_A = BM * BK, RAW_B = BN * BK;
   static constexpr int RAW_STAGE = (RAW_A + RAW_B + 127) / 128 * 128;
-  // ring depth: about 24 KB of raw stages in flight (4 to 16), so that the TMA round
-  // trip of a stage hides behind the stages before it
-  static constexpr int NS_ = 24576 / RAW_STAGE;
-  static constexpr int NS = NS_ < 4 ? 4 : (NS_ > 16 ? 16 : NS_);
+  // ring depth: a power of two (slot and phase by mask and shift), about 16-24 KB of
+  // raw stages in flight
+  static constexpr int NS = RAW_STAGE <= 1536 ? 16 : (RAW_STAGE <= 3072 ? 8 : 4);
   static constexpr int VROW = KP * 8 + 16;       // bytes per decoded row of values
   static constexpr int LROW = KP * 4 + 16;       // bytes per decoded row of labels
   static constexpr int VAL_BYTES = ROWS * VROW;
@@ -864,6 +835,7 @@ struct ChainShape {
   static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
   static_assert(NT % WPR_ == 0, "a thread decodes the same word position of every row it takes");
   static_assert(32 % LREP == 0, "table copies divide the warp");
+  static_assert(NS * RAW_STAGE >= 2048, "the raw ring stages the decode-table entries");
 };
 
 constexpr int kClampE32 = 117 << 23;               // keep the scale positive (Inf/NaN c)
@@ -893,39 +865,35 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int64_t n0 = (int64_t)blockIdx.x * BN;
   const int s = blockIdx.z;
 
-  for (int i = tid; i < 256 * LREP; i += NT) {
-    lutA[i] = lut_entry((uint32_t)(i / LREP), p.fmt_a, kPreA);
-    lutB[i] = lut_entry((uint32_t)(i / LREP), p.fmt_b, kPreB);
-  }
+  fill_luts<LREP, NT>(lutA, reinterpret_cast<uint32_t*>(smem), p.fmt_a, p.fmt_b, tid);
 
-  // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end)
-  const int64_t K = p.K;
+  // the chain of split s: k-tiles t_begin, t_begin + stride, ... (< t_end); stage st
+  // is sub-stage st % spt of the chain's tile st / spt (K < 2^31: 32-bit counts)
+  const int K = (int)p.K;
   const int kt = p.S == 1 ? BK : p.ktile;
-  const int64_t T = (K + kt - 1) / kt;
-  int64_t t_begin, t_end, t_stride;
+  const int T = (K + kt - 1) / kt;
+  int t_begin, t_end, t_stride;
   if (p.S == 1) { t_begin = 0; t_end = T; t_stride = 1; }
   else if (p.scheme == 0) {
-    const int64_t q = (T + p.S - 1) / p.S;
-    t_begin = (int64_t)s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
+    const int q = (T + p.S - 1) / p.S;
+    t_begin = s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
   } else { t_begin = s; t_end = T; t_stride = p.S; }
-  int64_t n_tiles = 0;
-  if (t_end > t_begin) n_tiles = (t_end - t_begin + t_stride - 1) / t_stride;
-  const int stages_per_tile = kt / BK;
-  int64_t n_stages = n_tiles * stages_per_tile;
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + t_stride - 1) / t_stride : 0;
+  const int spt = kt / BK;                 // stages per k-tile
+  int n_stages = n_tiles * spt;
   if (n_tiles > 0) {
-    const int64_t t_last = t_begin + (n_tiles - 1) * t_stride;
-    const int64_t rem_last = K - t_last * kt;
-    const int64_t len_last = rem_last < kt ? rem_last : kt;
-    n_stages -= stages_per_tile - (len_last + BK - 1) / BK;
+    const int t_last = t_begin + (n_tiles - 1) * t_stride;
+    const int len_last = K - t_last * kt < kt ? K - t_last * kt : kt;
+    n_stages -= spt - (len_last + BK - 1) / BK;
   }
-  auto stage_k = [&](int64_t st) -> int {
-    const int64_t tl = st / stages_per_tile;
-    return (int)((t_begin + tl * t_stride) * kt + (st % stages_per_tile) * BK);
+  auto stage_k = [&](int st) -> int {
+    if (spt == 1) return (t_begin + st * t_stride) * kt;
+    return (t_begin + (st / spt) * t_stride) * kt + (st % spt) * BK;
   };
-  int64_t issued = 0;
-  auto issue = [&](int64_t st) {
+  int issued = 0;
+  auto issue = [&](int st) {
     issued = st + 1;
-    const int slot = (int)(st % NS);
+    const int slot = st & (NS - 1);
     const uint32_t bar = bar0 + 8u * slot;
     const uint32_t dst = smem_u32(smem + slot * CS::RAW_STAGE);
     const int k = stage_k(st);
@@ -933,13 +901,13 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     tma_load_2d(dst, &tmA, k, (int)m0, bar);
     tma_load_2d(dst + CS::RAW_A, &tmB, k, (int)n0, bar);
   };
-  auto full_wait = [&](int64_t st) {
-    return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st % NS), (uint32_t)((st / NS) & 1), kWaitPolls);
+  auto full_wait = [&](int st) {
+    return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st & (NS - 1)), (uint32_t)((st / NS) & 1), kWaitPolls);
   };
-  auto give_up = [&](int64_t from) {
+  auto give_up = [&](int from) {
     atomicExch(&g_emu_device_status, kStatusWaitTimeout);
     if (tid == 0)
-      for (int64_t x = from; x < issued; ++x) (void)full_wait(x);
+      for (int x = from; x < issued; ++x) (void)full_wait(x);
   };
 
   // Decode.  Unit j of this thread is raw word dw of operand row dr0 + j * NT / WPR_
@@ -948,8 +916,8 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int dw = tid % WPR_, dr0 = tid / WPR_;
   constexpr int DR_STEP = NT / WPR_;
   const uint32_t* lutr = lutA + lane % LREP;            // this lane's copy of table A
-  auto decode_units = [&](int64_t st, int buf, int j0, int j1) {
-    const unsigned char* raw = smem + (int)(st % NS) * CS::RAW_STAGE + dr0 * BK + dw * 4;
+  auto decode_units = [&](int st, int buf, int j0, int j1) {
+    const unsigned char* raw = smem + (st & (NS - 1)) * CS::RAW_STAGE + dr0 * BK + dw * 4;
     unsigned char* vbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + dr0 * CS::VROW + dw * 16;
     unsigned char* lbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + CS::VAL_BYTES +
                            dr0 * CS::LROW + dw * 8;
@@ -968,7 +936,7 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           make_uint2(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410));
     }
   };
-  auto decode_piece = [&](int64_t st, int buf, int piece) {
+  auto decode_piece = [&](int st, int buf, int piece) {
     decode_units(st, buf, piece * CS::UPT / CS::NPIECE, (piece + 1) * CS::UPT / CS::NPIECE);
   };
 
@@ -1085,8 +1053,10 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     fence_mbar_init();
   }
   __syncthreads();                       // tables and barriers ready
-  if (tid == 0)
-    for (int64_t st = 0; st < NS && st < n_stages; ++st) issue(st);
+  if (tid == 0) {
+    fence_proxy_async();                 // the ring staged the tables (generic stores)
+    for (int st = 0; st < NS && st < n_stages; ++st) issue(st);
+  }
 
   bool timed_out = false;
   if (n_stages > 0) {
@@ -1103,8 +1073,8 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   if (n_stages > 0) prefetch(0, 0, xc, epc);
   // every stage but the last: the next stage's decode is dealt over the first NBLK - 1
   // block steps (a wait that gave up leaves garbage there; the barrier then ends the CTA)
-  for (int64_t st = 0; st + 1 < n_stages; ++st) {
-    const int cur = (int)(st & 1), nxt = cur ^ 1;
+  for (int st = 0; st + 1 < n_stages; ++st) {
+    const int cur = st & 1, nxt = cur ^ 1;
     timed_out = !full_wait(st + 1);
 #pragma unroll
     for (int bb = 0; bb + 1 < NBLK; ++bb) {
@@ -1120,7 +1090,7 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     step(xc, epc, true, nxt, 0);
   }
   if (n_stages > 0) {                    // the last stage
-    const int cur = (int)((n_stages - 1) & 1);
+    const int cur = (n_stages - 1) & 1;
 #pragma unroll
     for (int bb = 0; bb + 1 < NBLK; ++bb) step(xc, epc, true, cur, bb + 1);
     step(xc, epc, false, cur, 0);

@@ -99,11 +99,21 @@ def kernel_source_hash() -> str:
 
 
 def profile_summary(workload: str):
-    """The committed ncu summary of this workload's GEMM launch, if it was taken on
-    the current kernel sources: {"traffic": DRAM bytes per launch, "ncu": {...}}."""
-    path = os.path.join(ROOT, "profiles", f"emu_gemm_{workload}.md")
-    if not os.path.exists(path):
+    """The committed ncu summary of this workload's GEMM launch (profiles/<kernel>_<workload>.md,
+    the kernel emu_gemm or emu_chain), if it was taken on the current kernel sources:
+    {"traffic": DRAM bytes per launch, "ncu": {...}}."""
+    import glob
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", f"emu_*_{workload}.md")))
+    if not paths:
         return None
+    for path in paths:
+        got = _profile_fields(path)
+        if got is not None:
+            return got
+    return None
+
+
+def _profile_fields(path: str):
     fields, table = {}, {}
     with open(path) as f:
         for line in f:
@@ -613,7 +623,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="a workload case by name, or NAME@MxNxK: its recipe at those sizes")
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--shard", default="replicas", choices=("replicas", "columns"),
                     help="N > 1: whole workload per rank (weak) or column slabs of it (strong)")
@@ -628,7 +639,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cs = W.case(args.workload)
+    cs = W.named(args.workload)
     if args.impl == "reference":
         run_reference(args, cs)
     else:

@@ -153,3 +153,12 @@ def case(name: str) -> Case:
 def shrink(cs: Case, M: int, N: int, K: int) -> Case:
     """The same recipe at smaller sizes (for oracle-sized parity runs)."""
     return replace(cs, name=f"{cs.name}@{M}x{N}x{K}", M=M, N=N, K=K)
+
+
+def named(name: str) -> Case:
+    """A workload case by name; "NAME@MxNxK" is case NAME's recipe at those sizes."""
+    if "@" not in name:
+        return case(name)
+    base, sizes = name.split("@", 1)
+    M, N, K = (int(v) for v in sizes.split("x"))
+    return shrink(case(base), M, N, K)

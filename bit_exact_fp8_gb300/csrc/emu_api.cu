@@ -83,10 +83,10 @@ constexpr TileInfo kTiles[] = {
     {"K4H", 1, 2, 4, 16, 128, 4, 4, 128, 4, 26.0, 21.0, 21.0, 0.0, 1.0, true},
     // chain tiles (emu_chain_kernel): one output per lane group of g lanes; 128-code
     // stages for 32-product blocks, 64-code stages for 16-product blocks
-    {"C2", 1, 1, 8, 8, 128, 2, 2, 128, 2, 17.5, 12.0, 18.0, 13000.0, 1.0, false},
-    {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 53.0, 13.3, 20.6, 13000.0, 1.0, false},
-    {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 17.5, 14.0, 17.0, 10000.0, 1.0, false},
-    {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 12.5, 26.0, 26.5, 12000.0, 1.0, false},
+    {"C2", 1, 1, 8, 8, 128, 2, 2, 128, 2, 13.9, 10.1, 16.1, 2000.0, 1.0, false},
+    {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 20.0, 11.25, 19.8, 5700.0, 1.0, false},
+    {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 13.8, 12.55, 16.0, 3000.0, 1.0, false},
+    {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 8.5, 20.9, 21.7, 6800.0, 1.0, false},
 };
 constexpr int kNumTiles = 12;
 constexpr int kFirstChainTile = 8;
@@ -198,10 +198,10 @@ int launch_tile(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
               : launch_one<TM, TN, WM, WN, BK, 16, false, G, MINB, PK, LREP>(p, st);
 }
 
-template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB>
+template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB, bool PF>
 int launch_chain_one(const emu::GemmParams& p, cudaStream_t st) {
-  using CS = emu::ChainShape<BM, BN, G, BK, BLK, LREP>;
-  auto kern = emu::emu_chain_kernel<BM, BN, G, BK, BLK, SLOW, LREP, MINB>;
+  using CS = emu::ChainShape<BM, BN, G, BK, BLK, LREP, PF>;
+  auto kern = emu::emu_chain_kernel<BM, BN, G, BK, BLK, SLOW, LREP, MINB, PF>;
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);
@@ -227,14 +227,14 @@ int launch_chain_one(const emu::GemmParams& p, cudaStream_t st) {
 
 // chain tile BM x BN outputs, G lanes each: 128-code stages for 32-product blocks,
 // 64-code stages for 16-product blocks
-template <int BM, int BN, int G, int LREP, int MINB>
+template <int BM, int BN, int G, int LREP, int MINB, bool PF = false>
 int launch_chain(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   if (blk == 32) {
-    return slow ? launch_chain_one<BM, BN, G, 128, 32, true, LREP, MINB>(p, st)
-                : launch_chain_one<BM, BN, G, 128, 32, false, LREP, MINB>(p, st);
+    return slow ? launch_chain_one<BM, BN, G, 128, 32, true, LREP, MINB, PF>(p, st)
+                : launch_chain_one<BM, BN, G, 128, 32, false, LREP, MINB, PF>(p, st);
   }
-  return slow ? launch_chain_one<BM, BN, G, 64, 16, true, LREP, MINB>(p, st)
-              : launch_chain_one<BM, BN, G, 64, 16, false, LREP, MINB>(p, st);
+  return slow ? launch_chain_one<BM, BN, G, 64, 16, true, LREP, MINB, PF>(p, st)
+              : launch_chain_one<BM, BN, G, 64, 16, false, LREP, MINB, PF>(p, st);
 }
 
 // Pick the tile with the lowest estimated time in SM clocks: per K element of a
@@ -279,9 +279,9 @@ constexpr int LREP_M40 = 8, LREP_M32 = 8, LREP_M64 = 8, LREP_S = 2, LREP_K = 2;
 
 int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
   switch (choose_tile(p, blk, slow, sm_count())) {
-    case 8: return launch_chain<8, 8, 2, 32, 2>(p, blk, slow, st);
-    case 9: return launch_chain<8, 4, 4, 32, 2>(p, blk, slow, st);
-    case 10: return launch_chain<8, 8, 1, 8, 4>(p, blk, slow, st);
+    case 8: return launch_chain<8, 8, 2, 32, 2, true>(p, blk, slow, st);
+    case 9: return launch_chain<8, 4, 4, 32, 2, true>(p, blk, slow, st);
+    case 10: return launch_chain<8, 8, 1, 8, 4, true>(p, blk, slow, st);
     case 11: return launch_chain<16, 16, 1, 8, 2>(p, blk, slow, st);
     case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1, 1, true, LREP_M40>(p, blk, slow, st);
     case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, LREP_M32>(p, blk, slow, st);

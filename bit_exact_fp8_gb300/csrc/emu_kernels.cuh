@@ -15,7 +15,9 @@
 //   * Operands are decoded once per CTA and K-stage into shared memory as an fp32
 //     value pre-scaled by 2^-46 (A) or 2^-47 (B), so every exact product
 //     x' = a'b' = x * 2^-93 is a normal fp32, and as a 16-bit "label" (e + 17) << 7
-//     (zero codes: -16384, which never wins a maximum).
+//     (zero codes: -16384, which never wins a maximum).  The chain tiles keep the
+//     value as bf16 (exact: at most four significant bits) and take the exact
+//     product of a k-pair with one bf16x2 multiply.
 //   * The chain state is c' = c * 2^-93 (always normal or zero: a nonzero c is at
 //     least 2^-33 because every block grid is at least 2^(-20-13)).  Its upper 16
 //     bits, sign cleared, compare with the label sums: (e(c) + 34) << 7 | 7 fraction
@@ -134,6 +136,16 @@ __device__ __forceinline__ f32x2_t fadd2_rn(f32x2_t a, f32x2_t b) {
   f32x2_t r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
+}
+// Exact products of bf16 pairs, widened to an fp32 pair (low half first).  The
+// pre-scaled operand values have at most four significant bits and lie in
+// [2^-62, 2^-30] (A) and [2^-63, 2^-31] (B), so each product has at most eight
+// significant bits, the width of a bf16 significand, and lies in [2^-125, 2^-61],
+// inside bf16's normal range: the rounding never acts, and bf16 -> fp32 is a shift.
+__device__ __forceinline__ f32x2_t bmul2_exact(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return pack2(__uint_as_float(r << 16), __uint_as_float(r & 0xFFFF0000u));
 }
 
 // ---------------------------------------------------------------------------
@@ -791,15 +803,22 @@ emu_gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 // and its product-label maximum, group-reduced -- is done one block ahead, while
 // the previous block's c-dependent step (scale from max(E_p, e(c)), truncation,
 // sum, normalise) is in flight; the next stage's decode is dealt over the first
-// NBLK - 1 blocks of the current stage.  Decode tables hold one 32-bit entry per
-// code (the pre-scaled value in bits 31..20, the label in bits 15..0), replicated
-// LREP times so that the lanes of a warp read distinct banks.  Decoded rows (values
-// as k-pairs, labels as k-pair words) are padded by 16 bytes, so that each lane
-// reads its runs from its own base address with compile-time offsets and the rows
-// of a warp start in distinct bank quads.
-template <int BM_, int BN_, int G_, int BK_, int BLK_, int LREP_>
+// block steps of the current stage.  Decode tables hold one 32-bit entry per code
+// (the pre-scaled value in bits 31..20, the label in bits 15..0), replicated LREP
+// times so that the lanes of a warp read distinct banks.  A decoded row holds, per
+// two k-pairs, one 16-byte chunk: the two bf16 value pairs (the pre-scaled values
+// have at most four significant bits, so bf16 holds them exactly), then the two
+// label pairs; a lane's 16-byte load thus brings everything two of its k-pairs
+// need, a third fewer bytes than fp32 values beside the labels.  Rows are padded by
+// 16 bytes, so that each lane reads its runs from its own base address with
+// compile-time offsets and the rows of a warp start in distinct bank quads.  With PF
+// the operands of a block are loaded a whole block step before their products are
+// taken, and the decode's table lookups and stores bracket the step, so that no
+// instruction of the serial step waits in issue order behind a shared-memory load.
+template <int BM_, int BN_, int G_, int BK_, int BLK_, int LREP_, bool PF_ = false>
 struct ChainShape {
   static constexpr int BM = BM_, BN = BN_, G = G_, BK = BK_, BLK = BLK_, LREP = LREP_;
+  static constexpr bool PF = PF_;                // operands loaded one block step ahead
   static constexpr int GPW = 32 / G;             // lane groups (outputs) per warp
   static constexpr int WR = G == 4 ? 2 : 4;      // output rows of a warp
   static constexpr int WC = GPW / WR;            // output columns of a warp
@@ -814,11 +833,10 @@ struct ChainShape {
   // ring depth: a power of two (slot and phase by mask and shift), about 16-24 KB of
   // raw stages in flight
   static constexpr int NS = RAW_STAGE <= 1536 ? 16 : (RAW_STAGE <= 3072 ? 8 : 4);
-  static constexpr int VROW = KP * 8 + 16;       // bytes per decoded row of values
-  static constexpr int LROW = KP * 4 + 16;       // bytes per decoded row of labels
-  static constexpr int VAL_BYTES = ROWS * VROW;
-  static constexpr int LAB_BYTES = ROWS * LROW;
-  static constexpr int STAGE_BYTES = (VAL_BYTES + LAB_BYTES + 127) / 128 * 128;
+  // a decoded row: per two k-pairs one 16-byte chunk (bf16 value pairs of both, then
+  // their label pairs), and 16 bytes of pad
+  static constexpr int ROWB = KP * 8 + 16;
+  static constexpr int STAGE_BYTES = (ROWS * ROWB + 127) / 128 * 128;
   static constexpr int STAGE_OFF = NS * RAW_STAGE;
   static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
   static constexpr int LUT_BYTES = 2 * 256 * LREP * 4;
@@ -827,11 +845,15 @@ struct ChainShape {
   static constexpr int WPR_ = BK / 4;            // raw words (4 codes) per operand row
   static constexpr int UNITS = ROWS * WPR_;      // decode units: one raw word each
   static constexpr int UPT = (UNITS + NT - 1) / NT;
-  static constexpr int NPIECE = NBLK - 1;
+  // the next stage's decode is dealt over the first NPIECE block steps of a stage
+  // (with PF the barrier comes one step earlier, so that the step before the last can
+  // load the next stage's first block)
+  static constexpr int NPIECE = PF ? NBLK - 2 : NBLK - 1;
+  static constexpr int UPP = (UPT + NPIECE - 1) / NPIECE;   // units per piece, at most
   static_assert(G == 1 || G == 2 || G == 4, "lane groups of 1, 2 or 4");
   static_assert(NPL >= 2 && NPL % 2 == 0, "whole 16-byte value chunks per lane and block");
   static_assert(BM % WR == 0 && BN % WC == 0, "whole warps");
-  static_assert(NBLK >= 2, "the next stage's decode is dealt over the first NBLK - 1 blocks");
+  static_assert(NPIECE >= 1, "a stage has a block step for the next stage's decode");
   static_assert(RAW_A % 128 == 0, "the B box of a slot starts 128-byte aligned");
   static_assert(NT % WPR_ == 0, "a thread decodes the same word position of every row it takes");
   static_assert(32 % LREP == 0, "table copies divide the warp");
@@ -840,18 +862,17 @@ struct ChainShape {
 
 constexpr int kClampE32 = 117 << 23;               // keep the scale positive (Inf/NaN c)
 
-template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB>
+template <int BM, int BN, int G, int BK, int BLK, bool SLOW, int LREP, int MINB, bool PF = false>
 __global__ void __launch_bounds__(BM * BN * G, MINB)
 emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
                  const __grid_constant__ CUtensorMap tmB) {
-  using CS = ChainShape<BM, BN, G, BK, BLK, LREP>;
+  using CS = ChainShape<BM, BN, G, BK, BLK, LREP, PF>;
   constexpr int NT = CS::NT, NPB = CS::NPB, NPL = CS::NPL, NBLK = CS::NBLK;
   constexpr int NS = CS::NS, WPR_ = CS::WPR_;
 
   extern __shared__ __align__(128) unsigned char smem_dyn[];
   unsigned char* const smem = smem_dyn + ((128 - (smem_u32(smem_dyn) & 127)) & 127);
-  uint32_t* lutA = reinterpret_cast<uint32_t*>(smem + CS::LUT_OFF);
-  uint32_t* lutB = lutA + 256 * LREP;
+  uint32_t* lutA = reinterpret_cast<uint32_t*>(smem + CS::LUT_OFF);   // then B's table
   const uint32_t bar0 = smem_u32(smem + CS::BAR_OFF);
 
   const int tid = threadIdx.x;
@@ -916,11 +937,16 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int dw = tid % WPR_, dr0 = tid / WPR_;
   constexpr int DR_STEP = NT / WPR_;
   const uint32_t* lutr = lutA + lane % LREP;            // this lane's copy of table A
+  // one chunk from the table entries of 4 codes (two k-pairs): their values' upper 16
+  // bits (the bf16 value: entry bits 19..16 are zero) in pairs, then the label pairs
+  auto store_chunk = [](unsigned char* dst, const uint32_t (&e)[4]) {
+    *reinterpret_cast<uint4*>(dst) =
+        make_uint4(__byte_perm(e[0], e[1], 0x7632), __byte_perm(e[2], e[3], 0x7632),
+                   __byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410));
+  };
   auto decode_units = [&](int st, int buf, int j0, int j1) {
     const unsigned char* raw = smem + (st & (NS - 1)) * CS::RAW_STAGE + dr0 * BK + dw * 4;
-    unsigned char* vbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + dr0 * CS::VROW + dw * 16;
-    unsigned char* lbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + CS::VAL_BYTES +
-                           dr0 * CS::LROW + dw * 8;
+    unsigned char* cbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + dr0 * CS::ROWB + dw * 16;
 #pragma unroll
     for (int j = j0; j < j1; ++j) {
       const int r = dr0 + j * DR_STEP;
@@ -930,14 +956,46 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       uint32_t e[4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) e[b] = lut[__byte_perm(word, 0u, 0x4440u | b) * LREP];
-      *reinterpret_cast<uint4*>(vbase + j * DR_STEP * CS::VROW) =
-          make_uint4(e[0] & 0xFFF00000u, e[1] & 0xFFF00000u, e[2] & 0xFFF00000u, e[3] & 0xFFF00000u);
-      *reinterpret_cast<uint2*>(lbase + j * DR_STEP * CS::LROW) =
-          make_uint2(__byte_perm(e[0], e[1], 0x5410), __byte_perm(e[2], e[3], 0x5410));
+      store_chunk(cbase + j * DR_STEP * CS::ROWB, e);
     }
   };
   auto decode_piece = [&](int st, int buf, int piece) {
     decode_units(st, buf, piece * CS::UPT / CS::NPIECE, (piece + 1) * CS::UPT / CS::NPIECE);
+  };
+  // The same decode in three parts, for the prefetching steps: the raw words of all
+  // of a stage's units (a step before its first piece), the table lookups of one
+  // piece (at the start of a step) and its stores (at the end), so that a step's
+  // instructions never wait in order behind a decode load.
+  auto decode_raw = [&](int st, uint32_t (&w)[CS::UPT]) {
+    const unsigned char* raw = smem + (st & (NS - 1)) * CS::RAW_STAGE + dr0 * BK + dw * 4;
+#pragma unroll
+    for (int j = 0; j < CS::UPT; ++j) {
+      const int r = dr0 + j * DR_STEP;
+      w[j] = (CS::UNITS % NT != 0 && r >= CS::ROWS)
+                 ? 0u : *reinterpret_cast<const uint32_t*>(raw + j * DR_STEP * BK);
+    }
+  };
+  auto decode_lookup = [&](const uint32_t (&w)[CS::UPT], int piece, uint32_t (&e)[CS::UPP][4]) {
+    const int j0 = piece * CS::UPT / CS::NPIECE, j1 = (piece + 1) * CS::UPT / CS::NPIECE;
+#pragma unroll
+    for (int u = 0; u < CS::UPP; ++u) {
+      const int j = j0 + u;
+      if (j >= j1) break;
+      const uint32_t* lut = lutr + (dr0 + j * DR_STEP < BM ? 0 : 256 * LREP);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) e[u][b] = lut[__byte_perm(w[j], 0u, 0x4440u | b) * LREP];
+    }
+  };
+  auto decode_store = [&](int buf, int piece, const uint32_t (&e)[CS::UPP][4]) {
+    const int j0 = piece * CS::UPT / CS::NPIECE, j1 = (piece + 1) * CS::UPT / CS::NPIECE;
+    unsigned char* cbase = smem + CS::STAGE_OFF + buf * CS::STAGE_BYTES + dr0 * CS::ROWB + dw * 16;
+#pragma unroll
+    for (int u = 0; u < CS::UPP; ++u) {
+      const int j = j0 + u;
+      if (j >= j1) break;
+      if (CS::UNITS % NT != 0 && dr0 + j * DR_STEP >= CS::ROWS) continue;
+      store_chunk(cbase + j * DR_STEP * CS::ROWB, e[u]);
+    }
   };
 
   // Each lane reads its runs of a block from its own row bases.  One block step does
@@ -946,37 +1004,19 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // work of block b + 1: its exact products (packed k-pairs) and the group's label
   // maximum (bits 23..30: e_a + e_b + 34; negative: no nonzero product).
   const int lane_kp = gl * NPL;
-  const unsigned char* const vA0 = smem + CS::STAGE_OFF + ty * CS::VROW + lane_kp * 8;
-  const unsigned char* const vB0 = smem + CS::STAGE_OFF + (BM + tx) * CS::VROW + lane_kp * 8;
-  const unsigned char* const lA0 = smem + CS::STAGE_OFF + CS::VAL_BYTES + ty * CS::LROW + lane_kp * 4;
-  const unsigned char* const lB0 = smem + CS::STAGE_OFF + CS::VAL_BYTES + (BM + tx) * CS::LROW + lane_kp * 4;
-  auto load_labels = [&](int buf, int kb, uint32_t (&la)[NPL], uint32_t (&lb)[NPL]) {
-    const int off = buf * CS::STAGE_BYTES + kb * NPB * 4;
-    if constexpr (NPL % 4 == 0) {
-#pragma unroll
-      for (int i = 0; i < NPL / 4; ++i) {
-        const uint4 qa = *reinterpret_cast<const uint4*>(lA0 + off + i * 16);
-        const uint4 qb = *reinterpret_cast<const uint4*>(lB0 + off + i * 16);
-        la[4 * i] = qa.x; la[4 * i + 1] = qa.y; la[4 * i + 2] = qa.z; la[4 * i + 3] = qa.w;
-        lb[4 * i] = qb.x; lb[4 * i + 1] = qb.y; lb[4 * i + 2] = qb.z; lb[4 * i + 3] = qb.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < NPL / 2; ++i) {
-        const uint2 qa = *reinterpret_cast<const uint2*>(lA0 + off + i * 8);
-        const uint2 qb = *reinterpret_cast<const uint2*>(lB0 + off + i * 8);
-        la[2 * i] = qa.x; la[2 * i + 1] = qa.y; lb[2 * i] = qb.x; lb[2 * i + 1] = qb.y;
-      }
-    }
-  };
-  auto load_values = [&](int buf, int kb, f32x2_t (&va)[NPL], f32x2_t (&vb)[NPL]) {
+  const unsigned char* const rA0 = smem + CS::STAGE_OFF + ty * CS::ROWB + lane_kp * 8;
+  const unsigned char* const rB0 = smem + CS::STAGE_OFF + (BM + tx) * CS::ROWB + lane_kp * 8;
+  // this lane's operands of block kb in buffer buf: per k-pair the bf16 value pair
+  // and the label pair of its A row and of its B row
+  auto load_ops = [&](int buf, int kb, uint32_t (&va)[NPL], uint32_t (&la)[NPL],
+                      uint32_t (&vb)[NPL], uint32_t (&lb)[NPL]) {
     const int off = buf * CS::STAGE_BYTES + kb * NPB * 8;
 #pragma unroll
     for (int i = 0; i < NPL / 2; ++i) {
-      const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(vA0 + off + i * 16);
-      const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(vB0 + off + i * 16);
-      va[2 * i] = qa.x; va[2 * i + 1] = qa.y;
-      vb[2 * i] = qb.x; vb[2 * i + 1] = qb.y;
+      const uint4 qa = *reinterpret_cast<const uint4*>(rA0 + off + i * 16);
+      const uint4 qb = *reinterpret_cast<const uint4*>(rB0 + off + i * 16);
+      va[2 * i] = qa.x; va[2 * i + 1] = qa.y; la[2 * i] = qa.z; la[2 * i + 1] = qa.w;
+      vb[2 * i] = qb.x; vb[2 * i + 1] = qb.y; lb[2 * i] = qb.z; lb[2 * i + 1] = qb.w;
     }
   };
   // the group's maximum of the pass-1 accumulators, both halves, high half kept
@@ -989,14 +1029,12 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   };
   // block 0's c-independent work alone (no c-dependent step to interleave with)
   auto prefetch = [&](int buf, int kb, f32x2_t (&x2)[NPL], int& ep32) {
-    uint32_t la[NPL], lb[NPL];
-    f32x2_t va[NPL], vb[NPL];
-    load_labels(buf, kb, la, lb);
-    load_values(buf, kb, va, vb);
+    uint32_t la[NPL], lb[NPL], va[NPL], vb[NPL];
+    load_ops(buf, kb, va, la, vb, lb);
     uint32_t e0 = 0x80008000u, e1 = 0x80008000u;
 #pragma unroll
     for (int q = 0; q < NPL; ++q) {
-      x2[q] = fmul2_rn(va[q], vb[q]);
+      x2[q] = bmul2_exact(va[q], vb[q]);
       if (q & 1) e1 = __viaddmax_s16x2(la[q], lb[q], e1);
       else e0 = __viaddmax_s16x2(la[q], lb[q], e0);
     }
@@ -1009,12 +1047,8 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   // one block step: the c-dependent work of the block in (xc, epc) and, when next,
   // the c-independent work of block kb of buffer buf into (xc, epc) for the next step
   auto step = [&](f32x2_t (&xc)[NPL], int& epc, bool next, int buf, int kb) {
-    uint32_t la[NPL], lb[NPL];
-    f32x2_t va[NPL], vb[NPL];
-    if (next) {
-      load_labels(buf, kb, la, lb);
-      load_values(buf, kb, va, vb);
-    }
+    uint32_t la[NPL], lb[NPL], va[NPL], vb[NPL];
+    if (next) load_ops(buf, kb, va, la, vb, lb);
     int E = max(epc, (int)(__float_as_uint(c) & 0x7F800000u));
     E = min(E, kClampE32);
     const uint32_t sc = kScaleBase - (uint32_t)E;
@@ -1029,7 +1063,7 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
       if (q & 1) s1 = fadd2_rn(s1, t);
       else s0 = fadd2_rn(s0, t);
       if (next) {
-        xc[q] = fmul2_rn(va[q], vb[q]);
+        xc[q] = bmul2_exact(va[q], vb[q]);
         if (q & 1) e1 = __viaddmax_s16x2(la[q], lb[q], e1);
         else e0 = __viaddmax_s16x2(la[q], lb[q], e0);
       }
@@ -1045,6 +1079,56 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         c = 0.0f;
         bic = 0;
       }
+    }
+  };
+
+  // PF: the step loads the operands of the block after its next one, and takes the
+  // next block's products from the operands loaded by the step before it, so that a
+  // load has a whole block step to land
+  uint32_t la_n[NPL], lb_n[NPL];         // next block's operands (PF)
+  uint32_t va_n[NPL], vb_n[NPL];
+  uint32_t rw[CS::UPT];                  // raw words of the stage being decoded (PF)
+  auto step_pf = [&](f32x2_t (&xc)[NPL], int& epc, bool prod, bool load, int buf, int kb,
+                     int piece, int dbuf) {
+    uint32_t la[NPL], lb[NPL], va[NPL], vb[NPL];
+    if (load) load_ops(buf, kb, va, la, vb, lb);
+    uint32_t de[CS::UPP][4];
+    if (piece >= 0) decode_lookup(rw, piece, de);
+    int E = max(epc, (int)(__float_as_uint(c) & 0x7F800000u));
+    E = min(E, kClampE32);
+    const uint32_t sc = kScaleBase - (uint32_t)E;
+    const float scf = __uint_as_float(sc);
+    const f32x2_t sc2 = pack2(scf, scf);
+    f32x2_t s0 = pack2((G == 1 || gl == 0) ? fmul_rz(c, scf) : 0.0f, 0.0f);
+    f32x2_t s1 = pack2(0.0f, 0.0f);
+    uint32_t e0 = 0x80008000u, e1 = 0x80008000u;
+#pragma unroll
+    for (int q = 0; q < NPL; ++q) {
+      const f32x2_t t = fmul2_rz(xc[q], sc2);
+      if (q & 1) s1 = fadd2_rn(s1, t);
+      else s0 = fadd2_rn(s0, t);
+      if (prod) {
+        xc[q] = bmul2_exact(va_n[q], vb_n[q]);
+        if (q & 1) e1 = __viaddmax_s16x2(la_n[q], lb_n[q], e1);
+        else e0 = __viaddmax_s16x2(la_n[q], lb_n[q], e0);
+      }
+    }
+    float sum = sum_halves(fadd2_rn(s0, s1));
+    if (prod) epc = finish_ep(e0, e1);
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) sum = fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, off));
+    c = __uint_as_float(__float_as_uint(fmul_rn(sum, __uint_as_float(kInvBase - sc))) & kKeep14);
+    if (SLOW) {
+      if (++bic == p.restart_blocks) {
+        accs = fadd_rn(accs, fmul_rn(c, kTwo93));
+        c = 0.0f;
+        bic = 0;
+      }
+    }
+    if (piece >= 0) decode_store(dbuf, piece, de);
+    if (load) {
+#pragma unroll
+      for (int q = 0; q < NPL; ++q) { la_n[q] = la[q]; lb_n[q] = lb[q]; va_n[q] = va[q]; vb_n[q] = vb[q]; }
     }
   };
 
@@ -1071,6 +1155,41 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   f32x2_t xc[NPL];
   int epc = 0;
   if (n_stages > 0) prefetch(0, 0, xc, epc);
+  if constexpr (PF) {
+    // stage st: steps of blocks 0 .. NBLK - 3 (each with a piece of stage st + 1's
+    // decode) load blocks 2 .. NBLK - 1; the barrier; the last two steps load the next
+    // stage's blocks 0 and 1, and between them the raw words of stage st + 2 are read
+    if (n_stages > 0) {
+      load_ops(0, 1, va_n, la_n, vb_n, lb_n);
+    }
+    if (n_stages > 1) {
+      timed_out = !full_wait(1);
+      decode_raw(1, rw);
+    }
+    for (int st = 0; st + 1 < n_stages; ++st) {
+      const int cur = st & 1, nxt = cur ^ 1;
+#pragma unroll
+      for (int bb = 0; bb + 2 < NBLK; ++bb) step_pf(xc, epc, true, true, cur, bb + 2, bb, nxt);
+      if (__syncthreads_or(timed_out)) { give_up(st + 1); return; }
+      if (tid == 0 && st + 1 + NS < n_stages) {
+        fence_proxy_async();
+        issue(st + 1 + NS);
+      }
+      step_pf(xc, epc, true, true, nxt, 0, -1, 0);
+      if (st + 2 < n_stages) {
+        timed_out = !full_wait(st + 2);
+        decode_raw(st + 2, rw);
+      }
+      step_pf(xc, epc, true, true, nxt, 1, -1, 0);
+    }
+    if (n_stages > 0) {                  // the last stage
+      const int cur = (n_stages - 1) & 1;
+#pragma unroll
+      for (int bb = 0; bb + 2 < NBLK; ++bb) step_pf(xc, epc, true, true, cur, bb + 2, -1, 0);
+      step_pf(xc, epc, true, false, cur, 0, -1, 0);
+      step_pf(xc, epc, false, false, cur, 0, -1, 0);
+    }
+  } else {
   // every stage but the last: the next stage's decode is dealt over the first NBLK - 1
   // block steps (a wait that gave up leaves garbage there; the barrier then ends the CTA)
   for (int st = 0; st + 1 < n_stages; ++st) {
@@ -1094,6 +1213,7 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
     for (int bb = 0; bb + 1 < NBLK; ++bb) step(xc, epc, true, cur, bb + 1);
     step(xc, epc, false, cur, 0);
+  }
   }
 
   float res;

@@ -19,11 +19,14 @@ maximum over ranks.  SM clocks and throttle reasons are sampled through NVML eve
 Roofline: the denominators are measured in the same run by libemupeaks (the
 instruction rates of the pipes the kernel issues on, lane-operations per clock per
 SM) times the SM count and the maximum SM clock.  The headline fraction is against
-the rate at which the GB300 issues the kernel's own per-MAC arithmetic (1.5 packed
-f32x2 instructions and 0.5 DPX add-max); beside it the FP32 pipe alone, the
-algorithmic count of 5 integer lane-operations per MAC against the measured
-integer peak, and for the split-K shapes the HBM bytes against the measured HBM
-bandwidth and the serial-chain latency per block.
+the rate at which the GB300 runs the GEMM's own inner loop on a 4 x 4 thread tile
+(per output and k-pair 1.5 packed f32x2 instructions and 0.5 DPX add-max per MAC,
+operands loaded from shared memory, every operand a per-thread register); beside it
+the same arithmetic with operands shared by all threads (a register-file-light
+upper bound), the FP32 pipe alone, the algorithmic count of 5 integer
+lane-operations per MAC against the measured integer peak, and for the split-K
+shapes the HBM bytes against the measured HBM bandwidth and the serial-chain
+latency per block.
 
 CPU baseline and parity: the CPU oracle (exact integer arithmetic, every host
 thread) is timed on stripes of the same workload -- a 64-row stripe, then column
@@ -408,17 +411,28 @@ def roofline(cs, t_step, rates, peaks, sms, prof):
     macs = cs.M * cs.N * cs.K
     tflops = 2.0 * macs / t_step / 1e12
     mix = rates["emulation_mix_macs"]
+    vec = rates.get("emulation_mix_vector_macs")
+    tile = rates.get("emulation_tile_macs")
     packed = min(rates[k] for k in ("f32x2_fmul_rz_subnormal", "f32x2_fmul_rn_normal",
                                     "f32x2_fadd_subnormal"))
     int_peak = max(rates[k] for k in ("imad", "iadd3", "lop3", "prmt", "dpx_viaddmax_s16x2",
                                       "imad_iadd3_mixed"))
-    peak = 2.0 * mix * clk / 1e12
+    roof_macs = tile if tile else mix
+    peak = 2.0 * roof_macs * clk / 1e12
     roof = {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
             "frac": tflops / peak,
             "traffic": prof["traffic"] if prof else None,
-            "note": (f"peak = measured issue rate of the kernel's per-MAC arithmetic (1.5 packed "
-                     f"f32x2 + 0.5 DPX per MAC: {mix:.1f} MAC/clk/SM, libemupeaks in this run) "
-                     f"x {sms} SMs x {mhz:.0f} MHz (sm_max_mhz); achieved = 2MNK / event time")}
+            "note": (f"peak = measured rate of the GEMM's inner loop on a 4 x 4 thread tile "
+                     f"(per output and k-pair: packed exact product, truncating multiply and add, "
+                     f"and a DPX add-max; operands loaded from a decoded stage in shared memory; "
+                     f"no decode, scale or barrier): {roof_macs:.1f} MAC/clk/SM, libemupeaks in "
+                     f"this run, x {sms} SMs x {mhz:.0f} MHz (sm_max_mhz); achieved = 2MNK / "
+                     f"event time. The same arithmetic issues at {mix:.1f} MAC/clk/SM when its "
+                     f"second operands are the same in every thread"
+                     + (f", and at {vec:.1f} with per-thread operands and little reuse" if vec else "")
+                     + ": register-file reads, not the FP32 pipe, bound it")}
+    roof["uniform_operand_mix"] = {"macs_per_clk_sm": mix, "peak": 2.0 * mix * clk / 1e12,
+                                   "frac": tflops / (2.0 * mix * clk / 1e12)}
     roof["fp32_pipe"] = {"ops_per_mac": FP32_OPS_PER_MAC, "unit": "Tops/s",
                          "achieved": FP32_OPS_PER_MAC * macs / t_step / 1e12,
                          "peak": packed * clk / 1e12,

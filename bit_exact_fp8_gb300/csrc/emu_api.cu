@@ -87,12 +87,18 @@ constexpr TileInfo kTiles[] = {
     {"C4", 1, 1, 8, 4, 128, 2, 2, 128, 4, 20.0, 11.25, 19.8, 5700.0, 1.0, false},
     {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 13.8, 12.55, 16.0, 3000.0, 1.0, false},
     {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 8.5, 20.9, 21.7, 6800.0, 1.0, false},
+    // warp-specialised large tile (emu_ws_kernel): 512 consumer + 128 producer threads
+    {"W", 4, 4, 128, 64, 640, 1, 1, 32, 1, 4.72, 200.0, 200.0, 0.0, 1.0, false},
 };
-constexpr int kNumTiles = 12;
+constexpr int kNumTiles = 13;
 constexpr int kFirstChainTile = 8;
 // K-stage of a tile for blocks of blk products (the chain tiles stage 64 codes for
 // 16-product blocks)
-int tile_bk(int t, int blk) { return (t >= kFirstChainTile && blk == 16) ? 64 : kTiles[t].bk; }
+constexpr int kNumChainTiles = 4;
+int tile_bk(int t, int blk) {
+  const bool chain = t >= kFirstChainTile && t < kFirstChainTile + kNumChainTiles;
+  return (chain && blk == 16) ? 64 : kTiles[t].bk;
+}
 // SMs of the current device (152 on a GB300), cached per device (atomics: the entry
 // points may be called from several host threads)
 int sm_count() {
@@ -225,6 +231,41 @@ int launch_chain_one(const emu::GemmParams& p, cudaStream_t st) {
   return EMU_OK;
 }
 
+template <int BLK, bool SLOW, int LREP>
+int launch_ws_one(const emu::GemmParams& p, cudaStream_t st) {
+  using WS = emu::WsShape<LREP>;
+  using TS = typename WS::TS;
+  static_assert(WS::SMEM_BYTES + 1024 <= 228 * 1024, "one CTA per SM fits in shared memory");
+  auto kern = emu::emu_ws_kernel<BLK, SLOW, LREP>;
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WS::SMEM_BYTES);
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  CUtensorMap tmA, tmB;
+  int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK, TS::SWZ);
+  if (rc != EMU_OK) return rc;
+  rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK, TS::SWZ);
+  if (rc != EMU_OK) return rc;
+  const int64_t tiles_m = (p.M + TS::BM - 1) / TS::BM;
+  for (int64_t y0 = 0; y0 < tiles_m; y0 += 65535) {
+    emu::GemmParams q = p;
+    q.m_tile0 = y0;
+    const int64_t ny = tiles_m - y0 < 65535 ? tiles_m - y0 : 65535;
+    dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)ny, (unsigned)p.S);
+    kern<<<grid, WS::NTH, WS::SMEM_BYTES, st>>>(q, tmA, tmB);
+  }
+  return EMU_OK;
+}
+constexpr int LREP_W = 8;
+int launch_ws(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
+  if (blk == 32)
+    return slow ? launch_ws_one<32, true, LREP_W>(p, st) : launch_ws_one<32, false, LREP_W>(p, st);
+  return slow ? launch_ws_one<16, true, LREP_W>(p, st) : launch_ws_one<16, false, LREP_W>(p, st);
+}
+
 // chain tile BM x BN outputs, G lanes each: 128-code stages for 32-product blocks,
 // 64-code stages for 16-product blocks
 template <int BM, int BN, int G, int LREP, int MINB, bool PF = false>
@@ -283,6 +324,7 @@ int launch_gemm(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
     case 9: return launch_chain<8, 4, 4, 32, 2, true>(p, blk, slow, st);
     case 10: return launch_chain<8, 8, 1, 8, 4, true>(p, blk, slow, st);
     case 11: return launch_chain<16, 16, 1, 8, 2>(p, blk, slow, st);
+    case 12: return launch_ws(p, blk, slow, st);
     case 0: return launch_tile<4, 2, 16, 20, 128, 1, 1, 1, true, LREP_M40>(p, blk, slow, st);
     case 1: return launch_tile<4, 4, 16, 8, 32, 1, 3, 3, true, LREP_M32>(p, blk, slow, st);
     case 2: return launch_tile<2, 2, 8, 8, 64, 1, 6, 6, true, LREP_S>(p, blk, slow, st);

@@ -69,15 +69,22 @@ __device__ __forceinline__ u64 pk(float lo, float hi) {
 // The measured operations.  MIX: the GEMM's arithmetic mix per MAC, 1.5 packed
 // FP32 instructions (exact product, truncating multiply, exact add) and 0.5 DPX
 // add-max: per iteration six packed chains and two DPX chains, i.e. four MACs.
+// The modes above take their second and third operands from kernel arguments (the
+// same for every thread); the _vector modes take every operand from registers that
+// differ per thread, as the GEMM's operands do.  MIX_VEC: four outputs' exact
+// product, truncating multiply and add (each product fed by another output's sum)
+// and four DPX add-max of per-thread labels, i.e. eight MACs per iteration.
 enum Mode {
   FMUL_RZ_SUB, FMUL_RN, FADD_SUB, F2_FMUL_RZ_SUB, F2_FMUL_RN, F2_FADD_SUB,
-  DPX_VIADDMAX, IMAD, IADD3, LOP3, PRMT, IMAD_IADD3, MIX, NUM_MODES
+  DPX_VIADDMAX, IMAD, IADD3, LOP3, PRMT, IMAD_IADD3, MIX, DPX_VEC, F2_FMUL_RZ_VEC, MIX_VEC,
+  MIX_TILE, NUM_MODES
 };
 const char* const kNames[NUM_MODES] = {
     "fmul_rz_subnormal", "fmul_rn_normal", "fadd_subnormal",
     "f32x2_fmul_rz_subnormal", "f32x2_fmul_rn_normal", "f32x2_fadd_subnormal",
     "dpx_viaddmax_s16x2", "imad", "iadd3", "lop3", "prmt", "imad_iadd3_mixed",
-    "emulation_mix_macs"};
+    "emulation_mix_macs", "dpx_viaddmax_s16x2_vector", "f32x2_fmul_rz_subnormal_vector",
+    "emulation_mix_vector_macs", "emulation_tile_macs"};
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -94,6 +101,14 @@ probe(unsigned long long* cycles, unsigned* sink, float f0, float fk, unsigned u
   }
   const unsigned ku = u0 ^ 0x1234u, kv = u0 * 3u + 1u;
   const u64 k2 = pk(fk, fk);
+  unsigned wu[NCH], wv[NCH];             // per-thread operands of the _vector modes
+  u64 w2[NCH];
+#pragma unroll
+  for (int i = 0; i < NCH; ++i) {
+    wu[i] = ku + (unsigned)(threadIdx.x * 7 + i);
+    wv[i] = kv ^ (unsigned)(threadIdx.x * 13 + i);
+    w2[i] = pk(fk * (1.0f + 0.125f * (float)((threadIdx.x + i) & 3)), fk);
+  }
 #pragma unroll 1
   for (int it = 0; it < ITERS; ++it) {
 #pragma unroll
@@ -115,6 +130,16 @@ probe(unsigned long long* cycles, unsigned* sink, float f0, float fk, unsigned u
                                                                          : add_rn2(v[i], k2);
         else u[i] = __viaddmax_s16x2(u[i], ku, kv);
       }
+      if (MODE == DPX_VEC) u[i] = __viaddmax_s16x2(wu[i], wv[i], u[i]);
+      if (MODE == F2_FMUL_RZ_VEC) v[i] = mul_rz2(v[i], w2[i]);
+      if (MODE == MIX_VEC) {
+        if (i < 4) {
+          const u64 x = mul_rn2(v[(i + 1) & 3], w2[i]);
+          v[i] = add_rn2(v[i], mul_rz2(x, w2[i + 4]));
+        } else {
+          u[i] = __viaddmax_s16x2(wu[i], wv[i], u[i]);
+        }
+      }
     }
   }
   unsigned acc = 0;
@@ -126,11 +151,97 @@ probe(unsigned long long* cycles, unsigned* sink, float f0, float fk, unsigned u
   if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
 }
 
+// The GEMM's inner loop on a 4 x 4 thread tile: per k-pair the thread loads its
+// four A and four B value pairs and label pairs from a decoded stage in shared
+// memory (the 128 x 64 tile's layout), then per output one exact product,
+// truncating multiply and add (packed f32x2 on the k-pair) and one DPX add-max.  No
+// decode, no per-block scale or normalisation, no barrier: the ceiling of the
+// kernel's arithmetic and operand traffic.  512 threads per SM, the GEMM's budget of
+// 128 registers; 32 MACs per thread and k-pair.
+constexpr int TILE_THREADS = 512;
+constexpr int TILE_ITERS = 2048;
+__global__ void __launch_bounds__(TILE_THREADS, 1)
+probe_tile(unsigned long long* cycles, unsigned* sink, float f0, float fk, unsigned u0) {
+  __shared__ __align__(16) u64 sA[16][128];
+  __shared__ __align__(16) u64 sB[16][64];
+  __shared__ __align__(16) unsigned sAl[16][128];
+  __shared__ __align__(16) unsigned sBl[16][64];
+  for (int x = threadIdx.x; x < 16 * 128; x += TILE_THREADS) {
+    const int kp = x / 128, r = x % 128;
+    sA[kp][r] = pk(f0 * (float)(1 + (x & 7)), f0 * (float)(2 + (x & 3)));
+    sAl[kp][r] = u0 + (unsigned)x * 0x00010001u;
+    if (r < 64) {
+      sB[kp][r] = pk(fk * (float)(1 + (x & 3)), fk);
+      sBl[kp][r] = u0 ^ ((unsigned)x * 0x00030003u);
+    }
+  }
+  __syncthreads();
+  const unsigned long long t0 = clock64();
+  const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
+  u64 pa[4][4], sc2[4][4];
+  unsigned e2[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pa[i][j] = pk(f0, f0 * 0.5f);
+      sc2[i][j] = pk(fk * (float)(1 + ((i + j + threadIdx.x) & 3)), fk);
+      e2[i][j] = 0x80008000u;
+    }
+#pragma unroll 4
+  for (int it = 0; it < TILE_ITERS; ++it) {
+    const int kp = it & 15;
+    u64 a2[4], b2[4];
+    unsigned la[4], lb[4];
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+      const ulonglong2 va = *reinterpret_cast<const ulonglong2*>(&sA[kp][ty * 4 + i]);
+      a2[i] = va.x; a2[i + 1] = va.y;
+      const ulonglong2 vb = *reinterpret_cast<const ulonglong2*>(&sB[kp][tx * 2 + i * 16]);
+      b2[i] = vb.x; b2[i + 1] = vb.y;
+    }
+    const uint4 qa = *reinterpret_cast<const uint4*>(&sAl[kp][ty * 4]);
+    const uint4 qb = *reinterpret_cast<const uint4*>(&sBl[kp][tx * 4]);
+    la[0] = qa.x; la[1] = qa.y; la[2] = qa.z; la[3] = qa.w;
+    lb[0] = qb.x; lb[1] = qb.y; lb[2] = qb.z; lb[3] = qb.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        pa[i][j] = add_rn2(pa[i][j], mul_rz2(mul_rn2(a2[i], b2[j]), sc2[i][j]));
+        e2[i][j] = __viaddmax_s16x2(la[i], lb[j], e2[i][j]);
+      }
+  }
+  unsigned acc = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc ^= e2[i][j] ^ (unsigned)pa[i][j] ^ (unsigned)(pa[i][j] >> 32);
+  const unsigned long long t1 = clock64();
+  if (acc == 0xdeadbeefu) sink[threadIdx.x] = acc;
+  if (threadIdx.x == 0) cycles[blockIdx.x] = t1 - t0;
+}
+
+int run_tile(int nsm, unsigned long long* d_cyc, unsigned* d_sink, double* rate) {
+  probe_tile<<<nsm, TILE_THREADS>>>(d_cyc, d_sink, 1e-41f, 0.99999994f, 3u);   // warm-up
+  probe_tile<<<nsm, TILE_THREADS>>>(d_cyc, d_sink, 1e-41f, 0.99999994f, 3u);
+  if (cudaDeviceSynchronize() != cudaSuccess) return -4;
+  unsigned long long h[1024];
+  if (cudaMemcpy(h, d_cyc, nsm * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -4;
+  unsigned long long mx = 1;
+  for (int i = 0; i < nsm; ++i) mx = h[i] > mx ? h[i] : mx;
+  *rate = 32.0 * (double)TILE_THREADS * TILE_ITERS / (double)mx;
+  return 0;
+}
+
 // operations one iteration of one chain counts for, per mode
 double ops_per_chain_iter(int mode) {
   switch (mode) {
     case F2_FMUL_RZ_SUB: case F2_FMUL_RN: case F2_FADD_SUB: return 2.0;
+    case F2_FMUL_RZ_VEC: return 2.0;
     case MIX: return 4.0 / NCH;            // four MACs per iteration over all chains
+    case MIX_VEC: return 8.0 / NCH;        // eight MACs per iteration over all chains
     default: return 1.0;
   }
 }
@@ -219,6 +330,10 @@ int emu_peaks_measure(double* rates) {
   rc |= run_mode<PRMT>(nsm, d_cyc, d_sink, 1.0f, 1.0f, &rates[PRMT]);
   rc |= run_mode<IMAD_IADD3>(nsm, d_cyc, d_sink, 1.0f, 1.0f, &rates[IMAD_IADD3]);
   rc |= run_mode<MIX>(nsm, d_cyc, d_sink, 1e-41f, 0.99999994f, &rates[MIX]);
+  rc |= run_mode<DPX_VEC>(nsm, d_cyc, d_sink, 1.0f, 1.0f, &rates[DPX_VEC]);
+  rc |= run_mode<F2_FMUL_RZ_VEC>(nsm, d_cyc, d_sink, 1e-41f, 0.99999994f, &rates[F2_FMUL_RZ_VEC]);
+  rc |= run_mode<MIX_VEC>(nsm, d_cyc, d_sink, 1e-41f, 0.99999994f, &rates[MIX_VEC]);
+  rc |= run_tile(nsm, d_cyc, d_sink, &rates[MIX_TILE]);
   cudaFree(d_cyc);
   cudaFree(d_sink);
   return rc ? -4 : 0;

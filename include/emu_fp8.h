@@ -249,8 +249,8 @@ int emu_device_status(int32_t* status, int32_t reset);
 /*
  * The CTA tile the GEMM entry points launch for this problem (the format pair and
  * the output dtype do not enter the choice), by its name: "M40", "M32", "M64",
- * "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1" or "C1L", or "none" when M, N or
- * K is 0.  The choice is
+ * "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L" or "W", or "none" when M,
+ * N or K is 0.  The choice is
  * this library's cost model of the GB300 (an estimate per tile of issue and
  * latency time, fitted to measurements), not a behaviour of the pages' platforms;
  * every tile gives the same bits.  sm_count > 0 stands in for the device's SM

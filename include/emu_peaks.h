@@ -23,14 +23,20 @@ int emu_peaks_count(void);
 
 /* Name of operation i ("" when out of range): fmul_rz_subnormal, fmul_rn_normal,
    fadd_subnormal, their f32x2_ forms, dpx_viaddmax_s16x2, imad, iadd3, lop3, prmt,
-   imad_iadd3_mixed, emulation_mix_macs. */
+   imad_iadd3_mixed, emulation_mix_macs, dpx_viaddmax_s16x2_vector,
+   f32x2_fmul_rz_subnormal_vector, emulation_mix_vector_macs, emulation_tile_macs. */
 const char* emu_peaks_name(int i);
 
 /* rates[i] (emu_peaks_count() doubles, caller-owned host memory): lane-operations per
    clock per SM of operation i, from one CTA of 1024 threads per SM each running 8
    independent chains (a packed f32x2 instruction counts two operations);
    emulation_mix_macs: MACs per clock per SM of the GEMM's per-MAC arithmetic, 1.5
-   packed f32x2 instructions and 0.5 DPX add-max.  Returns 0, or -4 on a CUDA error. */
+   packed f32x2 instructions and 0.5 DPX add-max.  The operations without _vector
+   take their second and third operands from kernel arguments, the same in every
+   thread; the _vector ones take all operands from per-thread registers, as the GEMM
+   does (emulation_mix_vector_macs: the same mix so fed); emulation_tile_macs: MACs
+   per clock per SM of the GEMM's inner loop on a 4 x 4 thread tile from registers
+   (512 threads per SM).  Returns 0, or -4 on a CUDA error. */
 int emu_peaks_measure(double* rates);
 
 /* bad[0..2] (3 caller-owned unsigned ints): halves of n random operand pairs on which

@@ -46,8 +46,10 @@ def test_peaks_library_exports_every_declared_symbol(lib):
                         "emu_peaks_f32x2_agreement"}
     for name in declared:
         assert hasattr(L, name), name
-    assert L.emu_peaks_count() == 13
-    assert L.emu_peaks_name(12) == b"emulation_mix_macs" and L.emu_peaks_name(13) == b""
+    assert L.emu_peaks_count() == 17
+    assert L.emu_peaks_name(12) == b"emulation_mix_macs"
+    assert L.emu_peaks_name(15) == b"emulation_mix_vector_macs"
+    assert L.emu_peaks_name(16) == b"emulation_tile_macs" and L.emu_peaks_name(17) == b""
 
 
 def test_presets_and_abi(lib):

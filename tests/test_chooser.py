@@ -18,9 +18,10 @@ MEASURED_BEST = [
     ((16, 64, 256, True, 1, "hopper"), {"K8H", "C2", "C4"}),  # the small case
     ((64, 5760, 1920, True, 1, "hopper"), {"M40"}),           # linear layer
     ((64, 5760, 1920, False, 1, "hopper"), {"M40"}),
-    ((4096, 4096, 4096, False, 1, "hopper"), {"M32"}),        # square, slow
-    ((8192, 5760, 1920, True, 1, "hopper"), {"M64"}),         # projections
-    ((8192, 1920, 1920, True, 1, "hopper"), {"M64"}),
+    ((4096, 4096, 4096, False, 1, "hopper"), {"W"}),          # square, slow
+    ((8192, 5760, 1920, True, 1, "hopper"), {"W"}),           # projections
+    ((8192, 1920, 1920, True, 1, "hopper"), {"W"}),
+    ((2048, 5760, 1920, True, 1, "hopper"), {"W"}),
     ((16, 256, 262144, True, 2, "hopper"), {"C2"}),           # split-K
     ((16, 256, 262144, False, 2, "hopper"), {"C2"}),
     ((16, 256, 262144, True, 2, "ada"), {"C1", "C2"}),
@@ -41,6 +42,7 @@ MEASURED_BEST = [
     ((48, 5760, 1920, True, 1, "hopper"), {"M40"}),
     ((128, 5760, 1920, True, 1, "hopper"), {"M40"}),
     ((256, 5760, 1920, True, 1, "hopper"), {"M32"}),
+    ((384, 5760, 1920, True, 1, "hopper"), {"W"}),
     ((512, 5760, 1920, True, 1, "hopper"), {"M64"}),
 ]
 

@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdlib>
@@ -88,7 +89,7 @@ constexpr TileInfo kTiles[] = {
     {"C1", 1, 1, 8, 8, 64, 4, 4, 128, 1, 13.8, 12.55, 16.0, 3000.0, 1.0, false},
     {"C1L", 1, 1, 16, 16, 256, 2, 2, 128, 1, 8.5, 20.9, 21.7, 6800.0, 1.0, false},
     // warp-specialised large tile (emu_ws_kernel): 512 consumer + 128 producer threads
-    {"W", 4, 4, 128, 64, 640, 1, 1, 32, 1, 4.72, 200.0, 200.0, 0.0, 1.0, false},
+    {"W", 4, 4, 128, 64, 640, 1, 1, 32, 1, 4.41, 200.0, 200.0, 0.0, 1.065, false},
 };
 constexpr int kNumTiles = 13;
 constexpr int kFirstChainTile = 8;
@@ -231,12 +232,18 @@ int launch_chain_one(const emu::GemmParams& p, cudaStream_t st) {
   return EMU_OK;
 }
 
+// the W tile: slow chains on emu_ws_kernel (the producers take every block's label
+// maximum), fast chains on emu_wsp_kernel (the consumers take it only where it can
+// exceed e(c))
 template <int BLK, bool SLOW, int LREP>
 int launch_ws_one(const emu::GemmParams& p, cudaStream_t st) {
-  using WS = emu::WsShape<LREP>;
+  using WS = typename std::conditional<SLOW, emu::WsShape<LREP>, emu::WspShape<LREP>>::type;
   using TS = typename WS::TS;
   static_assert(WS::SMEM_BYTES + 1024 <= 228 * 1024, "one CTA per SM fits in shared memory");
-  auto kern = emu::emu_ws_kernel<BLK, SLOW, LREP>;
+  auto kern = [] {
+    if constexpr (SLOW) return emu::emu_ws_kernel<BLK, SLOW, LREP>;
+    else return emu::emu_wsp_kernel<BLK, SLOW, LREP>;
+  }();
   static std::atomic<bool> configured[64];
   int dev = 0;
   cudaGetDevice(&dev);

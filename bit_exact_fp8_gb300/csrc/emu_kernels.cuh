@@ -1244,8 +1244,10 @@ emu_chain_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 }
 
 // ---------------------------------------------------------------------------
-// Warp-specialised tile for the large shapes: 128 x 64 outputs per CTA, one CTA per
-// SM.  Sixteen consumer warps hold 4 x 4 outputs per thread and run only the
+// Warp-specialised tile for the large shapes, slow chains: 128 x 64 outputs per CTA,
+// one CTA per SM.  (Fast chains take emu_wsp_kernel below, which needs the label
+// maximum only where it can matter; a slow chain restarts from c = 0 every few
+// blocks, so there it nearly always does.)  Sixteen consumer warps hold 4 x 4 outputs per thread and run only the
 // c-dependent step of each block (scale, pass 2, normalise) on the FP32 pipe; four
 // producer warps, one per scheduler, decode each K-stage and take every block's
 // product-label maximum E_p (pass 1, DPX on the integer pipe) one or two blocks
@@ -1563,6 +1565,390 @@ emu_ws_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
     }
     __syncwarp();
     if ((tid & 31) == 0) mbar_arrive(empty0 + 8u * (uint32_t)(b & 1));
+  }
+
+  // chain results
+  float res[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 c4 = cst[i * NC];
+    const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+    float av[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (SLOW) {
+      const float4 a4 = acs[i * NC];
+      av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      res[i][j] = SLOW ? (bic ? fadd_rn(av[j], fmul_rn(cv[j], kTwo93)) : av[j]) : fmul_rn(cv[j], kTwo93);
+  }
+  if (p.S > 1) {
+    float* dst = p.partial + (int64_t)s * p.M * p.N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t m = m0 + ty * 4 + i;
+      if (m >= p.M) continue;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t n = n0 + tx * 4 + j;
+        if (n < p.N) dst[m * p.N + n] = res[i][j];
+      }
+    }
+    return;
+  }
+  const float alpha = fmul_rn(__ldg(p.scale_a), __ldg(p.scale_b));
+  const OutStore store(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t m = m0 + ty * 4 + i;
+    if (m >= p.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t n = n0 + tx * 4 + j;
+      if (n >= p.N) continue;
+      store(p, m * p.N + n, fma_plus0(res[i][j], alpha));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Warp-specialised tile for the large shapes, fast chains: 128 x 64 outputs per CTA,
+// one CTA per SM.  Four producer warps, one per scheduler, decode each K-stage: values in the
+// packed layout of the GEMM kernel, label pairs row by row, and the label maximum of
+// every 16-code chunk of every row.  Sixteen consumer warps hold 4 x 4 outputs per
+// thread and run the blocks.  A block's alignment exponent E = max(E_p, e(c)) needs
+// the product-label maximum E_p only where it can exceed e(c): the chunk maxima give
+// the bound U = max_k la + max_k lb >= E_p, and where U <= e(c), E = e(c) exactly.
+// On the workloads' data that holds for about nine outputs in ten once the chains
+// have grown, so each warp gathers its outputs with U > e(c) into a list and its
+// lanes share the list, one output each, for the exact maximum (DPX add-max over the
+// block's label pairs); the FP32 pass over the block's products then follows for
+// every output.  Stages are handed over by mbarriers (FULL: producers to consumers;
+// EMPTY: back), every wait is bounded, and a wait that gives up ends both sides.
+// The chain states c' (and the slow chains' sums) live in shared memory between
+// blocks, which keeps the consumers within the register budget of 640 threads.
+template <int LREP_>
+struct WspShape {
+  using TS = TileShape<4, 4, 32, 16, 32, 1, LREP_>;
+  static constexpr int BM = TS::BM, BN = TS::BN, BK = TS::BK;
+  static constexpr int NC = TS::NT;                // consumer threads (16 warps)
+  static constexpr int NP = 128;                   // producer threads (4 warps)
+  static constexpr int NTH = NC + NP;
+  static constexpr int OUT = BM * BN;              // outputs per CTA
+  static constexpr int KPR = BK / 2;               // k-pairs per row and stage
+  static constexpr int LROW = KPR + 4;             // words per row of label pairs (padded)
+  // one decoded stage: packed values (the GEMM kernel's layout), label pairs row by
+  // row (A rows, then B rows), chunk maxima [BK / 16][row] (A, then B)
+  static constexpr int V_BYTES = (BK * BM + BK * BN) * 4;
+  static constexpr int L_OFF = V_BYTES;
+  static constexpr int M_OFF = L_OFF + (BM + BN) * LROW * 4;
+  static constexpr int STAGE_BYTES = (M_OFF + (BK / 16) * (BM + BN) * 4 + 127) / 128 * 128;
+  static constexpr int STAGE_OFF = TS::NS * TS::RAW_STAGE;
+  static constexpr int LUT_OFF = STAGE_OFF + 2 * STAGE_BYTES;
+  static constexpr int WBAR_OFF = LUT_OFF + 2 * 256 * LREP_ * 4;   // NS raw + FULL[2] + EMPTY[2]
+  static constexpr int LIST_OFF = (WBAR_OFF + (TS::NS + 4) * 8 + 127) / 128 * 128;
+  static constexpr int LIST_BYTES = 32 * 16 * 2;   // per consumer warp: its outputs, u16 each
+  static constexpr int RES_OFF = LIST_OFF + (NC / 32) * LIST_BYTES;
+  static constexpr int CST_OFF = RES_OFF + (NC / 32) * LIST_BYTES;
+  static constexpr int ACC_OFF = CST_OFF + OUT * 4;
+  static constexpr int SMEM_BYTES = ACC_OFF + OUT * 4 + TS::RAW_ALIGN;
+  static_assert(TS::SWZ && TS::RAW_A % TS::RAW_ALIGN == 0, "swizzled raw boxes");
+  static_assert((BM * BK / 16) % NP == 0 && (BN * BK / 16) % NP == 0, "whole chunk rounds");
+};
+
+template <int BLK, bool SLOW, int LREP>
+__global__ void __launch_bounds__(WspShape<LREP>::NTH, 1)
+emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
+              const __grid_constant__ CUtensorMap tmB) {
+  using WS = WspShape<LREP>;
+  using TS = typename WS::TS;
+  constexpr int TN = 4, WN = 16;
+  constexpr int BM = WS::BM, BN = WS::BN, BK = WS::BK, NS = TS::NS;
+  constexpr int NC = WS::NC, NP = WS::NP, KPR = WS::KPR, LROW = WS::LROW;
+  constexpr int NBLK = BK / BLK, NPB = BLK / 2;     // blocks per stage, k-pairs per block
+  constexpr int A_CHUNKS = BM * BK / 16, B_CHUNKS = BN * BK / 16;
+  constexpr int AB_PER = (A_CHUNKS + B_CHUNKS) / NP;
+  static_assert(BK % BLK == 0 && BLK % 16 == 0, "blocks of whole 16-code chunks");
+  auto b_slot = [](int n) { return ((n % TN) / 2) * (2 * WN) + (n / TN) * 2 + (n % 2); };
+
+  extern __shared__ __align__(128) unsigned char smem_dyn[];
+  unsigned char* const smem =
+      smem_dyn + ((TS::RAW_ALIGN - (smem_u32(smem_dyn) & (TS::RAW_ALIGN - 1))) & (TS::RAW_ALIGN - 1));
+  uint32_t* lutA = reinterpret_cast<uint32_t*>(smem + WS::LUT_OFF);
+  uint32_t* lutB = lutA + 256 * LREP;
+  const uint32_t bar0 = smem_u32(smem + WS::WBAR_OFF);     // raw ring
+  const uint32_t full0 = bar0 + 8u * NS, empty0 = full0 + 16u;
+  const int tid = threadIdx.x;
+  const int64_t m0 = ((int64_t)blockIdx.y + p.m_tile0) * BM;
+  const int64_t n0 = (int64_t)blockIdx.x * BN;
+  const int s = blockIdx.z;
+  fill_luts<LREP, WS::NTH>(lutA, reinterpret_cast<uint32_t*>(smem), p.fmt_a, p.fmt_b, tid);
+
+  // the chain of split s (as in the GEMM kernel)
+  const int K = (int)p.K;
+  const int kt = p.S == 1 ? BK : p.ktile;
+  const int T = (K + kt - 1) / kt;
+  int t_begin, t_end, t_stride;
+  if (p.S == 1) { t_begin = 0; t_end = T; t_stride = 1; }
+  else if (p.scheme == 0) {
+    const int q = (T + p.S - 1) / p.S;
+    t_begin = s * q; t_end = t_begin + q < T ? t_begin + q : T; t_stride = 1;
+  } else { t_begin = s; t_end = T; t_stride = p.S; }
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + t_stride - 1) / t_stride : 0;
+  const int spt = kt / BK;
+  int n_stages = n_tiles * spt;
+  if (n_tiles > 0) {
+    const int t_last = t_begin + (n_tiles - 1) * t_stride;
+    const int len_last = K - t_last * kt < kt ? K - t_last * kt : kt;
+    n_stages -= spt - (len_last + BK - 1) / BK;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) mbar_init(bar0 + 8u * i, 1u);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(full0 + 8u * i, NP / 32);      // one arrival per producer warp
+      mbar_init(empty0 + 8u * i, NC / 32);     // one arrival per consumer warp
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();                             // tables and barriers ready
+
+  if (tid >= NC) {
+    // ---- producers: decode each stage into buffer st & 1
+    const int pt = tid - NC;
+    auto stage_k = [&](int st) -> int {
+      if (spt == 1) return (t_begin + st * t_stride) * kt;
+      return (t_begin + (st / spt) * t_stride) * kt + (st % spt) * BK;
+    };
+    int issued = 0;
+    auto issue = [&](int st) {
+      issued = st + 1;
+      const int slot = st % NS;
+      const uint32_t bar = bar0 + 8u * slot;
+      const uint32_t dst = smem_u32(smem + slot * TS::RAW_STAGE);
+      const int k = stage_k(st);
+      mbar_arrive_expect_tx(bar, (uint32_t)(TS::RAW_A + TS::RAW_B));
+      tma_load_2d(dst, &tmA, k, (int)m0, bar);
+      tma_load_2d(dst + TS::RAW_A, &tmB, k, (int)n0, bar);
+    };
+    auto raw_wait = [&](int st) {
+      return mbar_wait_bounded(bar0 + 8u * (uint32_t)(st % NS), (uint32_t)((st / NS) & 1), kWaitPolls);
+    };
+    auto give_up = [&](int from) {
+      atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+      if (pt == 0)
+        for (int x = from; x < issued; ++x) (void)raw_wait(x);
+    };
+    if (pt == 0) {
+      fence_proxy_async();                     // the ring staged the tables (generic stores)
+      for (int st = 0; st < NS && st < n_stages; ++st) issue(st);
+    }
+    const uint32_t* lA = lutA + (tid % 32) % LREP;
+    const uint32_t* lB = lutB + (tid % 32) % LREP;
+    for (int st = 0; st < n_stages; ++st) {
+      // the raw stage has landed, and the consumers are done with stage st - 2 (the
+      // last one in this buffer)
+      bool ok = raw_wait(st);
+      if (st >= 2)
+        ok = mbar_wait_bounded(empty0 + 8u * (uint32_t)(st & 1), (uint32_t)(((st - 2) >> 1) & 1),
+                               kWaitPolls) && ok;
+      if (named_sync_or(1, NP, !ok)) { give_up(st); return; }
+      const unsigned char* raw = smem + (st % NS) * TS::RAW_STAGE;
+      unsigned char* base = smem + WS::STAGE_OFF + (st & 1) * WS::STAGE_BYTES;
+      float* sAv = reinterpret_cast<float*>(base);
+      float* sBv = reinterpret_cast<float*>(base + BK * BM * 4);
+      uint32_t* sL = reinterpret_cast<uint32_t*>(base + WS::L_OFF);    // row r: A rows, B rows
+      int* sMx = reinterpret_cast<int*>(base + WS::M_OFF);             // [h][row]
+      constexpr int HM = BK / 16 - 1;
+      const uint32_t raw_u32 = smem_u32(raw);
+      // chunk c: 16 codes of row (A rows first); with the swizzle, chunk h of a box
+      // row sits at 16-byte position h XOR bits 7.. of the row's address
+#pragma unroll
+      for (int r = 0; r < AB_PER; ++r) {
+        const int c = pt + r * NP;
+        const bool isA = r * NP < A_CHUNKS;    // A_CHUNKS is a multiple of NP
+        const int cb = isA ? c : c - A_CHUNKS;
+        const int rows = isA ? BM : BN;
+        const int row = cb % rows, h = cb / rows;
+        const int off_row = isA ? row * BK : TS::RAW_A + row * BK;
+        const int hs = h ^ (int)(((raw_u32 + (uint32_t)off_row) >> 7) & (uint32_t)HM);
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + off_row + hs * 16);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        const uint32_t* lt = isA ? lA : lB;
+        uint32_t lp[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const uint32_t e0 = lt[__byte_perm(w[j >> 2], 0u, 0x4440u | (j & 3)) * LREP];
+          const uint32_t e1 = lt[__byte_perm(w[j >> 2], 0u, 0x4440u | ((j + 1) & 3)) * LREP];
+          const uint2 v = make_uint2(e0 & 0xFFF00000u, e1 & 0xFFF00000u);
+          lp[j / 2] = __byte_perm(e0, e1, 0x5410);
+          if (isA) *reinterpret_cast<uint2*>(sAv + ((h * 8 + j / 2) * BM + row) * 2) = v;
+          else *reinterpret_cast<uint2*>(sBv + ((h * 8 + j / 2) * BN + b_slot(row)) * 2) = v;
+        }
+        uint32_t* lrow = sL + (isA ? row : BM + row) * LROW + h * 8;
+        *reinterpret_cast<uint4*>(lrow) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+        *reinterpret_cast<uint4*>(lrow + 4) = make_uint4(lp[4], lp[5], lp[6], lp[7]);
+        uint32_t mx = __vmaxs2(__vmaxs2(__vmaxs2(lp[0], lp[1]), __vmaxs2(lp[2], lp[3])),
+                               __vmaxs2(__vmaxs2(lp[4], lp[5]), __vmaxs2(lp[6], lp[7])));
+        mx = __vmaxs2(mx, __byte_perm(mx, 0u, 0x1032));
+        sMx[h * (BM + BN) + (isA ? row : BM + row)] = (int)mx >> 16;    // the chunk's maximum label
+      }
+      named_sync(1, NP);                       // decoded; the raw slot is free
+      if (pt == 0 && st + NS < n_stages) {
+        fence_proxy_async();
+        issue(st + NS);
+      }
+      __syncwarp();
+      if ((pt & 31) == 0) mbar_arrive(full0 + 8u * (uint32_t)(st & 1));
+    }
+    return;
+  }
+
+  // ---- consumers
+  const int lane = tid & 31, warp = tid >> 5;
+  const int ty = tid / WN, tx = tid % WN;
+  float4* const cst = reinterpret_cast<float4*>(smem + WS::CST_OFF) + tid;   // rows i: + i * NC
+  float4* const acs = reinterpret_cast<float4*>(smem + WS::ACC_OFF) + tid;
+  uint16_t* const list = reinterpret_cast<uint16_t*>(smem + WS::LIST_OFF + warp * WS::LIST_BYTES);
+  uint16_t* const ep_res = reinterpret_cast<uint16_t*>(smem + WS::RES_OFF + warp * WS::LIST_BYTES);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    cst[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (SLOW) acs[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  int bic = 0;                                 // slow: blocks in the current chunk
+  for (int st = 0; st < n_stages; ++st) {
+    if (!mbar_wait_bounded(full0 + 8u * (uint32_t)(st & 1), (uint32_t)((st >> 1) & 1), kWaitPolls)) {
+      atomicExch(&g_emu_device_status, kStatusWaitTimeout);
+      return;
+    }
+    const unsigned char* base = smem + WS::STAGE_OFF + (st & 1) * WS::STAGE_BYTES;
+    const f32x2_t* pAv = reinterpret_cast<const f32x2_t*>(base);
+    const f32x2_t* pBv = reinterpret_cast<const f32x2_t*>(base + BK * BM * 4);
+    const uint32_t* sL = reinterpret_cast<const uint32_t*>(base + WS::L_OFF);
+    const int* sMx = reinterpret_cast<const int*>(base + WS::M_OFF);
+#pragma unroll 1
+    for (int bb = 0; bb < NBLK; ++bb) {
+      float cv[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 c4 = cst[i * NC];
+        cv[i][0] = c4.x; cv[i][1] = c4.y; cv[i][2] = c4.z; cv[i][3] = c4.w;
+      }
+      // the bound U = (row maximum + column maximum of the block's labels) against
+      // e(c), both in label units ((e + 34) << 7)
+      int ra[4] = {-32768, -32768, -32768, -32768}, rb[4] = {-32768, -32768, -32768, -32768};
+#pragma unroll
+      for (int h = bb * (BLK / 16); h < (bb + 1) * (BLK / 16); ++h) {
+        const int4 xa = *reinterpret_cast<const int4*>(sMx + h * (BM + BN) + ty * 4);
+        const int4 xb = *reinterpret_cast<const int4*>(sMx + h * (BM + BN) + BM + tx * 4);
+        ra[0] = max(ra[0], xa.x); ra[1] = max(ra[1], xa.y); ra[2] = max(ra[2], xa.z); ra[3] = max(ra[3], xa.w);
+        rb[0] = max(rb[0], xb.x); rb[1] = max(rb[1], xb.y); rb[2] = max(rb[2], xb.z); rb[3] = max(rb[3], xb.w);
+      }
+      uint32_t need = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ce = (int)((__float_as_uint(cv[i][j]) >> 16) & 0x7F80u);
+          if (ra[i] + rb[j] > ce) need |= 1u << (i * 4 + j);
+        }
+      // the warp's list of outputs that need E_p, then one output per lane
+      const int cnt = __popc(need);
+      int incl = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+      int idx = incl - cnt;
+      for (uint32_t m = need; m; m &= m - 1) list[idx++] = (uint16_t)(lane * 16 + __ffs(m) - 1);
+      __syncwarp();
+      for (int it = lane; it < total; it += 32) {
+        const int item = list[it];
+        const int ot = warp * 32 + (item >> 4), o = item & 15;
+        const int ml = (ot / WN) * 4 + (o >> 2), nl = (ot % WN) * 4 + (o & 3);
+        const uint32_t* la = sL + ml * LROW + bb * NPB;
+        const uint32_t* lb = sL + (BM + nl) * LROW + bb * NPB;
+        uint32_t e2 = 0x80008000u;
+#pragma unroll
+        for (int q = 0; q < NPB; q += 4) {
+          const uint4 a4 = *reinterpret_cast<const uint4*>(la + q);
+          const uint4 b4 = *reinterpret_cast<const uint4*>(lb + q);
+          e2 = __viaddmax_s16x2(a4.x, b4.x, e2);
+          e2 = __viaddmax_s16x2(a4.y, b4.y, e2);
+          e2 = __viaddmax_s16x2(a4.z, b4.z, e2);
+          e2 = __viaddmax_s16x2(a4.w, b4.w, e2);
+        }
+        e2 = __vmaxs2(e2, __byte_perm(e2, 0u, 0x1032));
+        ep_res[item] = (uint16_t)(e2 >> 16);
+      }
+      __syncwarp();
+      const uint4 r01 = *reinterpret_cast<const uint4*>(ep_res + lane * 16);
+      const uint4 r23 = *reinterpret_cast<const uint4*>(ep_res + lane * 16 + 8);
+      const uint32_t rw[8] = {r01.x, r01.y, r01.z, r01.w, r23.x, r23.y, r23.z, r23.w};
+      // scales 2^(-43-E), E = max(E_p, e(c)) clamped; E_p only where it may matter
+      f32x2_t sc2[4][4], pa[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int o = i * 4 + j;
+          const uint32_t w = rw[o >> 1];
+          const int epj = (need >> o) & 1u ? (int)((o & 1) ? (w & 0xFFFF0000u) : (w << 16))
+                                           : (int)0x80000000;
+          int E = max(epj, (int)(__float_as_uint(cv[i][j]) & 0x7F800000u));
+          E = min(E, kClampE32);
+          const float scf = __uint_as_float(kScaleBase - (uint32_t)E);
+          sc2[i][j] = pack2(scf, scf);
+          pa[i][j] = pack2(fmul_rz(cv[i][j], scf), 0.0f);
+        }
+#pragma unroll
+      for (int q = 0; q < NPB; ++q) {
+        const int kp = bb * NPB + q;
+        f32x2_t a2[4], b2[4];
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(pAv + kp * BM + ty * 4 + i);
+          a2[i] = v.x;
+          a2[i + 1] = v.y;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(pBv + kp * BN + b_slot(tx * 4 + j));
+          b2[j] = v.x;
+          b2[j + 1] = v.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            pa[i][j] = fadd2_rn(pa[i][j], fmul2_rz(fmul2_rn(a2[i], b2[j]), sc2[i][j]));
+      }
+      // normalise: c' = S * 2^(E-13) * 2^-93, truncated to 14 significant bits
+      const bool restart = SLOW && ++bic == p.restart_blocks;
+      if (restart) bic = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float cn[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float inv = __uint_as_float(kInvBase - lo_bits(sc2[i][j]));
+          cn[j] = __uint_as_float(__float_as_uint(fmul_rn(sum_halves(pa[i][j]), inv)) & kKeep14);
+        }
+        if (restart) {
+          const float4 a4 = acs[i * NC];
+          acs[i * NC] = make_float4(fadd_rn(a4.x, fmul_rn(cn[0], kTwo93)), fadd_rn(a4.y, fmul_rn(cn[1], kTwo93)),
+                                    fadd_rn(a4.z, fmul_rn(cn[2], kTwo93)), fadd_rn(a4.w, fmul_rn(cn[3], kTwo93)));
+          cst[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else {
+          cst[i * NC] = make_float4(cn[0], cn[1], cn[2], cn[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8u * (uint32_t)(st & 1));
   }
 
   // chain results

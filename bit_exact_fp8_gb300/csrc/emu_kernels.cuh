@@ -1845,64 +1845,81 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
         ra[0] = max(ra[0], xa.x); ra[1] = max(ra[1], xa.y); ra[2] = max(ra[2], xa.z); ra[3] = max(ra[3], xa.w);
         rb[0] = max(rb[0], xb.x); rb[1] = max(rb[1], xb.y); rb[2] = max(rb[2], xb.z); rb[3] = max(rb[3], xb.w);
       }
+      // two outputs (j, j + 1) per word, in 16-bit halves: the label form of c (its
+      // exponent field) and the bound; the chunk maxima are at least -16384 (a zero
+      // code's label), so the bound's sum stays within 16 bits
+      uint32_t c16[4][2];
       uint32_t need = 0;
+      const uint32_t rbp[2] = {__byte_perm((uint32_t)rb[0], (uint32_t)rb[1], 0x5410),
+                               __byte_perm((uint32_t)rb[2], (uint32_t)rb[3], 0x5410)};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t rap = __byte_perm((uint32_t)ra[i], 0u, 0x1010);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int ce = (int)((__float_as_uint(cv[i][j]) >> 16) & 0x7F80u);
-          if (ra[i] + rb[j] > ce) need |= 1u << (i * 4 + j);
+        for (int jp = 0; jp < 2; ++jp) {
+          c16[i][jp] = __byte_perm(__float_as_uint(cv[i][2 * jp]), __float_as_uint(cv[i][2 * jp + 1]),
+                                   0x7632) & 0x7F807F80u;
+          const uint32_t gt = __vcmpgts2(__vadd2(rap, rbp[jp]), c16[i][jp]);   // 0xFFFF where U > e(c)
+          need |= ((gt & 1u) | ((gt >> 15) & 2u)) << (i * 4 + 2 * jp);
         }
-      // the warp's list of outputs that need E_p, then one output per lane
-      const int cnt = __popc(need);
-      int incl = cnt;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if (lane >= d) incl += v;
       }
-      const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
-      int idx = incl - cnt;
-      for (uint32_t m = need; m; m &= m - 1) list[idx++] = (uint16_t)(lane * 16 + __ffs(m) - 1);
+      // the warp's list of outputs that need E_p (offsets from a ballot per bit of the
+      // counts), then one output per lane; every other output's entry stays -32768
+      const int cnt = __popc(need);
+      int before = 0, total = 0;
+#pragma unroll
+      for (int bit = 0; bit < 5; ++bit) {
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, (cnt >> bit) & 1);
+        before += __popc(bal & ((1u << lane) - 1u)) << bit;
+        total += __popc(bal) << bit;
+      }
+      uint4* const own = reinterpret_cast<uint4*>(ep_res + lane * 16);
+      own[0] = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+      own[1] = own[0];
+      for (uint32_t m = need; m; m &= m - 1) list[before++] = (uint16_t)(lane * 16 + __ffs(m) - 1);
       __syncwarp();
-      for (int it = lane; it < total; it += 32) {
-        const int item = list[it];
+      // the exact maximum of one listed output: four independent add-max chains
+      auto ep_of = [&](int item) -> uint16_t {
         const int ot = warp * 32 + (item >> 4), o = item & 15;
         const int ml = (ot / WN) * 4 + (o >> 2), nl = (ot % WN) * 4 + (o & 3);
         const uint32_t* la = sL + ml * LROW + bb * NPB;
         const uint32_t* lb = sL + (BM + nl) * LROW + bb * NPB;
-        uint32_t e2 = 0x80008000u;
+        uint32_t e[4] = {0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u};
 #pragma unroll
         for (int q = 0; q < NPB; q += 4) {
           const uint4 a4 = *reinterpret_cast<const uint4*>(la + q);
           const uint4 b4 = *reinterpret_cast<const uint4*>(lb + q);
-          e2 = __viaddmax_s16x2(a4.x, b4.x, e2);
-          e2 = __viaddmax_s16x2(a4.y, b4.y, e2);
-          e2 = __viaddmax_s16x2(a4.z, b4.z, e2);
-          e2 = __viaddmax_s16x2(a4.w, b4.w, e2);
+          e[0] = __viaddmax_s16x2(a4.x, b4.x, e[0]);
+          e[1] = __viaddmax_s16x2(a4.y, b4.y, e[1]);
+          e[2] = __viaddmax_s16x2(a4.z, b4.z, e[2]);
+          e[3] = __viaddmax_s16x2(a4.w, b4.w, e[3]);
         }
-        e2 = __vmaxs2(e2, __byte_perm(e2, 0u, 0x1032));
-        ep_res[item] = (uint16_t)(e2 >> 16);
+        uint32_t x = __vmaxs2(__vmaxs2(e[0], e[1]), __vmaxs2(e[2], e[3]));
+        x = __vmaxs2(x, __byte_perm(x, 0u, 0x1032));
+        return (uint16_t)(x >> 16);
+      };
+      for (int it = lane; it < total; it += 32) {
+        const int item = list[it];
+        ep_res[item] = ep_of(item);
       }
       __syncwarp();
-      const uint4 r01 = *reinterpret_cast<const uint4*>(ep_res + lane * 16);
-      const uint4 r23 = *reinterpret_cast<const uint4*>(ep_res + lane * 16 + 8);
+      const uint4 r01 = own[0], r23 = own[1];
       const uint32_t rw[8] = {r01.x, r01.y, r01.z, r01.w, r23.x, r23.y, r23.z, r23.w};
-      // scales 2^(-43-E), E = max(E_p, e(c)) clamped; E_p only where it may matter
+      // scales 2^(-43-E), E = max(E_p, e(c)) clamped, two outputs (j, j + 1) at a time
+      // in 16-bit halves: the label form of c (exponent field) against E_p
       f32x2_t sc2[4][4], pa[4][4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int o = i * 4 + j;
-          const uint32_t w = rw[o >> 1];
-          const int epj = (need >> o) & 1u ? (int)((o & 1) ? (w & 0xFFFF0000u) : (w << 16))
-                                           : (int)0x80000000;
-          int E = max(epj, (int)(__float_as_uint(cv[i][j]) & 0x7F800000u));
-          E = min(E, kClampE32);
-          const float scf = __uint_as_float(kScaleBase - (uint32_t)E);
-          sc2[i][j] = pack2(scf, scf);
-          pa[i][j] = pack2(fmul_rz(cv[i][j], scf), 0.0f);
+        for (int jp = 0; jp < 2; ++jp) {
+          const int j = 2 * jp;
+          const uint32_t e16 = __vmins2(__vmaxs2(rw[i * 2 + jp], c16[i][jp]), 0x3A803A80u);
+          const float s0 = __uint_as_float(kScaleBase - (e16 << 16));
+          const float s1 = __uint_as_float(kScaleBase - (e16 & 0xFFFF0000u));
+          sc2[i][j] = pack2(s0, s0);
+          sc2[i][j + 1] = pack2(s1, s1);
+          pa[i][j] = pack2(fmul_rz(cv[i][j], s0), 0.0f);
+          pa[i][j + 1] = pack2(fmul_rz(cv[i][j + 1], s1), 0.0f);
         }
 #pragma unroll
       for (int q = 0; q < NPB; ++q) {

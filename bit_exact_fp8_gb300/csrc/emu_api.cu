@@ -242,7 +242,7 @@ int launch_ws_one(const emu::GemmParams& p, cudaStream_t st) {
   static_assert(WS::SMEM_BYTES + 1024 <= 228 * 1024, "one CTA per SM fits in shared memory");
   auto kern = [] {
     if constexpr (SLOW) return emu::emu_ws_kernel<BLK, SLOW, LREP>;
-    else return emu::emu_wsp_kernel<BLK, SLOW, LREP>;
+    else return emu::emu_wsp_kernel<BLK, LREP>;
   }();
   static std::atomic<bool> configured[64];
   int dev = 0;

@@ -1625,8 +1625,8 @@ emu_ws_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 // block's label pairs); the FP32 pass over the block's products then follows for
 // every output.  Stages are handed over by mbarriers (FULL: producers to consumers;
 // EMPTY: back), every wait is bounded, and a wait that gives up ends both sides.
-// The chain states c' (and the slow chains' sums) live in shared memory between
-// blocks, which keeps the consumers within the register budget of 640 threads.
+// The chain states c' live in shared memory between blocks, which keeps the consumers
+// within the register budget of 640 threads.  Fast chains only.
 template <int LREP_>
 struct WspShape {
   using TS = TileShape<4, 4, 32, 16, 32, 1, LREP_>;
@@ -1650,13 +1650,12 @@ struct WspShape {
   static constexpr int LIST_BYTES = 32 * 16 * 2;   // per consumer warp: its outputs, u16 each
   static constexpr int RES_OFF = LIST_OFF + (NC / 32) * LIST_BYTES;
   static constexpr int CST_OFF = RES_OFF + (NC / 32) * LIST_BYTES;
-  static constexpr int ACC_OFF = CST_OFF + OUT * 4;
-  static constexpr int SMEM_BYTES = ACC_OFF + OUT * 4 + TS::RAW_ALIGN;
+  static constexpr int SMEM_BYTES = CST_OFF + OUT * 4 + TS::RAW_ALIGN;
   static_assert(TS::SWZ && TS::RAW_A % TS::RAW_ALIGN == 0, "swizzled raw boxes");
   static_assert((BM * BK / 16) % NP == 0 && (BN * BK / 16) % NP == 0, "whole chunk rounds");
 };
 
-template <int BLK, bool SLOW, int LREP>
+template <int BLK, int LREP>
 __global__ void __launch_bounds__(WspShape<LREP>::NTH, 1)
 emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
               const __grid_constant__ CUtensorMap tmB) {
@@ -1664,7 +1663,7 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   using TS = typename WS::TS;
   constexpr int TN = 4, WN = 16;
   constexpr int BM = WS::BM, BN = WS::BN, BK = WS::BK, NS = TS::NS;
-  constexpr int NC = WS::NC, NP = WS::NP, KPR = WS::KPR, LROW = WS::LROW;
+  constexpr int NC = WS::NC, NP = WS::NP, LROW = WS::LROW;
   constexpr int NBLK = BK / BLK, NPB = BLK / 2;     // blocks per stage, k-pairs per block
   constexpr int A_CHUNKS = BM * BK / 16, B_CHUNKS = BN * BK / 16;
   constexpr int AB_PER = (A_CHUNKS + B_CHUNKS) / NP;
@@ -1808,15 +1807,12 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
   const int lane = tid & 31, warp = tid >> 5;
   const int ty = tid / WN, tx = tid % WN;
   float4* const cst = reinterpret_cast<float4*>(smem + WS::CST_OFF) + tid;   // rows i: + i * NC
-  float4* const acs = reinterpret_cast<float4*>(smem + WS::ACC_OFF) + tid;
   uint16_t* const list = reinterpret_cast<uint16_t*>(smem + WS::LIST_OFF + warp * WS::LIST_BYTES);
   uint16_t* const ep_res = reinterpret_cast<uint16_t*>(smem + WS::RES_OFF + warp * WS::LIST_BYTES);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     cst[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (SLOW) acs[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
-  int bic = 0;                                 // slow: blocks in the current chunk
   for (int st = 0; st < n_stages; ++st) {
     if (!mbar_wait_bounded(full0 + 8u * (uint32_t)(st & 1), (uint32_t)((st >> 1) & 1), kWaitPolls)) {
       atomicExch(&g_emu_device_status, kStatusWaitTimeout);
@@ -1944,8 +1940,6 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
             pa[i][j] = fadd2_rn(pa[i][j], fmul2_rz(fmul2_rn(a2[i], b2[j]), sc2[i][j]));
       }
       // normalise: c' = S * 2^(E-13) * 2^-93, truncated to 14 significant bits
-      const bool restart = SLOW && ++bic == p.restart_blocks;
-      if (restart) bic = 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         float cn[4];
@@ -1954,14 +1948,7 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
           const float inv = __uint_as_float(kInvBase - lo_bits(sc2[i][j]));
           cn[j] = __uint_as_float(__float_as_uint(fmul_rn(sum_halves(pa[i][j]), inv)) & kKeep14);
         }
-        if (restart) {
-          const float4 a4 = acs[i * NC];
-          acs[i * NC] = make_float4(fadd_rn(a4.x, fmul_rn(cn[0], kTwo93)), fadd_rn(a4.y, fmul_rn(cn[1], kTwo93)),
-                                    fadd_rn(a4.z, fmul_rn(cn[2], kTwo93)), fadd_rn(a4.w, fmul_rn(cn[3], kTwo93)));
-          cst[i * NC] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        } else {
-          cst[i * NC] = make_float4(cn[0], cn[1], cn[2], cn[3]);
-        }
+        cst[i * NC] = make_float4(cn[0], cn[1], cn[2], cn[3]);
       }
     }
     __syncwarp();
@@ -1973,15 +1960,10 @@ emu_wsp_kernel(const GemmParams p, const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float4 c4 = cst[i * NC];
-    const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
-    float av[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    if (SLOW) {
-      const float4 a4 = acs[i * NC];
-      av[0] = a4.x; av[1] = a4.y; av[2] = a4.z; av[3] = a4.w;
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      res[i][j] = SLOW ? (bic ? fadd_rn(av[j], fmul_rn(cv[j], kTwo93)) : av[j]) : fmul_rn(cv[j], kTwo93);
+    res[i][0] = fmul_rn(c4.x, kTwo93);
+    res[i][1] = fmul_rn(c4.y, kTwo93);
+    res[i][2] = fmul_rn(c4.z, kTwo93);
+    res[i][3] = fmul_rn(c4.w, kTwo93);
   }
   if (p.S > 1) {
     float* dst = p.partial + (int64_t)s * p.M * p.N;

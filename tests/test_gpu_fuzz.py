@@ -12,7 +12,7 @@ import pytest
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-TILES = ["auto", "M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H"]
+TILES = ["auto", "M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L", "W"]
 
 CHILD = r'''
 import sys

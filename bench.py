@@ -83,7 +83,8 @@ def measured_peaks():
     return None
 
 
-KERNEL_SOURCES = ("bit_exact_fp8_gb300/csrc/emu_kernels.cuh", "bit_exact_fp8_gb300/csrc/emu_api.cu")
+KERNEL_SOURCES = ("bit_exact_fp8_gb300/csrc/emu_kernels.cuh", "bit_exact_fp8_gb300/csrc/emu_tc.cuh",
+                  "bit_exact_fp8_gb300/csrc/emu_api.cu")
 
 
 def kernel_source_hash() -> str:

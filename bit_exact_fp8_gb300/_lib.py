@@ -27,7 +27,7 @@ EMU_OUT_E5M2 = 4
 EXPORTED = ("emu_preset_get", "emu_workspace_bytes", "emu_scaled_mm", "emu_last_error",
             "emu_abi_version", "emu_scaled_mm_noalloc", "emu_device_status",
             "emu_selftest_wait_timeout", "emu_scaled_mm_ex", "emu_host_staging_bytes",
-            "emu_scaled_mm_host", "emu_tile_for")
+            "emu_scaled_mm_host", "emu_tile_for", "emu_tc_selftest")
 
 #: size of the static scratch of emu_scaled_mm_noalloc (EMU_NOALLOC_SCRATCH_BYTES)
 EMU_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -85,6 +85,8 @@ def load(path: str = LIB) -> ctypes.CDLL:
     L.emu_scaled_mm_host.restype = ctypes.c_int
     L.emu_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
     L.emu_device_status.restype = ctypes.c_int
+    L.emu_tc_selftest.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.emu_tc_selftest.restype = ctypes.c_int
     L.emu_selftest_wait_timeout.argtypes = [P]
     L.emu_selftest_wait_timeout.restype = ctypes.c_int
     L.emu_tile_for.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
@@ -168,6 +170,16 @@ def emu_device_status(reset: bool = False) -> int:
     st = load().emu_device_status(ctypes.byref(v), int(bool(reset)))
     if st != EMU_OK:
         raise RuntimeError(f"emu_device_status failed: {emu_last_error()}")
+    return int(v.value)
+
+
+def emu_tc_selftest() -> int:
+    """Outputs of the tensor-core product self-test that differ from the exact product
+    (0: exact), 0xFFFFFFFF if a wait gave up; raises on a CUDA error."""
+    v = ctypes.c_uint32(0)
+    st = load().emu_tc_selftest(ctypes.byref(v))
+    if st != EMU_OK:
+        raise RuntimeError(f"emu_tc_selftest failed: {emu_last_error()}")
     return int(v.value)
 
 

@@ -5,6 +5,7 @@
 // synchronises with the device or allocates device memory.
 #include "emu_fp8.h"
 #include "emu_kernels.cuh"
+#include "emu_tc.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -18,6 +19,8 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+
+int tc_selftest_impl(uint32_t* mismatches);   // the tensor-core product self-test
 
 namespace {
 
@@ -267,7 +270,60 @@ int launch_ws_one(const emu::GemmParams& p, cudaStream_t st) {
   return EMU_OK;
 }
 constexpr int LREP_W = 8;
+// W with tensor-core products (fast chains, 32-product blocks, E4M3FN A)
+int launch_wst(const emu::GemmParams& p, cudaStream_t st) {
+  using WS = emu::WtShape<LREP_W>;
+  using TS = typename WS::TS;
+  static_assert(WS::SMEM_BYTES + 1024 <= 228 * 1024, "one CTA per SM fits in shared memory");
+  auto kern = emu::emu_wst_kernel<LREP_W>;
+  static std::atomic<bool> configured[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WS::SMEM_BYTES);
+    if (dev >= 0 && dev < 64) configured[dev].store(true, std::memory_order_release);
+  }
+  CUtensorMap tmA, tmB;
+  int rc = make_operand_map(&tmA, p.A, p.M, p.K, TS::BM, TS::BK, TS::SWZ);
+  if (rc != EMU_OK) return rc;
+  rc = make_operand_map(&tmB, p.B, p.N, p.K, TS::BN, TS::BK, TS::SWZ);
+  if (rc != EMU_OK) return rc;
+  const int64_t tiles_m = (p.M + TS::BM - 1) / TS::BM;
+  for (int64_t y0 = 0; y0 < tiles_m; y0 += 65535) {
+    emu::GemmParams q = p;
+    q.m_tile0 = y0;
+    const int64_t ny = tiles_m - y0 < 65535 ? tiles_m - y0 : 65535;
+    dim3 grid((unsigned)((p.N + TS::BN - 1) / TS::BN), (unsigned)ny, (unsigned)p.S);
+    kern<<<grid, WS::NTH, WS::SMEM_BYTES, st>>>(q, tmA, tmB);
+  }
+  return EMU_OK;
+}
+// The tensor-core products are opt-in (EMU_FP8_TC=1): the W kernel with them is
+// bit-exact but slower than the register-file W kernel on these shapes (its
+// consumer warps move in lockstep with one MMA stream, so the sparse label-maximum
+// pass of every block runs with the tensor core idle).  Then a gate, once per
+// device: emu_tc_selftest must find every product exact.  Never run inside a stream
+// capture (the call is then served without the tensor cores).
+bool tc_products_ok(cudaStream_t st) {
+  static const bool on = [] {
+    const char* e = getenv("EMU_FP8_TC");
+    return e != nullptr && e[0] == '1' && e[1] == '\0';
+  }();
+  static std::atomic<int> gate[64];                 // 0 unknown, 1 exact, 2 not
+  if (!on) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const int v = gate[dev].load(std::memory_order_acquire);
+  if (v) return v == 1;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return false;
+  uint32_t mism = 1;
+  const bool ok = tc_selftest_impl(&mism) == EMU_OK && mism == 0;
+  gate[dev].store(ok ? 1 : 2, std::memory_order_release);
+  return ok;
+}
 int launch_ws(const emu::GemmParams& p, int blk, bool slow, cudaStream_t st) {
+  if (!slow && blk == 32 && p.fmt_a == 0 && tc_products_ok(st)) return launch_wst(p, st);
   if (blk == 32)
     return slow ? launch_ws_one<32, true, LREP_W>(p, st) : launch_ws_one<32, false, LREP_W>(p, st);
   return slow ? launch_ws_one<16, true, LREP_W>(p, st) : launch_ws_one<16, false, LREP_W>(p, st);
@@ -769,6 +825,57 @@ int emu_tile_for(int64_t M, int64_t N, int64_t K, int32_t fast_accum, int32_t sp
   std::strcpy(name, t);
   return EMU_OK;
 }
+
+int emu_tc_selftest(uint32_t* mismatches) {
+  g_last_error.clear();
+  if (!mismatches) return fail(EMU_EINVAL, "mismatches is null");
+  return tc_selftest_impl(mismatches);
+}
+
+}  // extern "C"
+
+int tc_selftest_impl(uint32_t* mismatches) {
+  cudaGetLastError();
+  unsigned* d_bad = nullptr;
+  int* d_status = nullptr;
+  if (cudaMalloc(&d_bad, sizeof(unsigned)) != cudaSuccess ||
+      cudaMalloc(&d_status, sizeof(int)) != cudaSuccess) {
+    cudaFree(d_bad);
+    return fail(EMU_ECUDA, "cudaMalloc failed");
+  }
+  int rc = EMU_OK;
+  unsigned bad = 0;
+  int status = 0;
+  cudaStream_t ts = nullptr;
+  if (cudaStreamCreateWithFlags(&ts, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(d_bad);
+    cudaFree(d_status);
+    return fail(EMU_ECUDA, "cudaStreamCreate failed");
+  }
+  if (cudaMemset(d_bad, 0, sizeof(unsigned)) != cudaSuccess ||
+      cudaMemset(d_status, 0, sizeof(int)) != cudaSuccess ||
+      cudaFuncSetAttribute(emu::emu_tc_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           emu::kTcSmem) != cudaSuccess) {
+    rc = fail(EMU_ECUDA, "self-test setup failed");
+  } else {
+    for (int fa = 0; fa < 2; ++fa)
+      for (int fb = 0; fb < 2; ++fb)
+        for (int r = 0; r < 2; ++r)
+          emu::emu_tc_selftest_kernel<<<1, 128, emu::kTcSmem, ts>>>(fa, fb, r, d_bad, d_status);
+    const cudaError_t e = cudaStreamSynchronize(ts);
+    if (e != cudaSuccess ||
+        cudaMemcpy(&bad, d_bad, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(&status, d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+      rc = fail(EMU_ECUDA, "self-test failed: %s", cudaGetErrorString(e));
+  }
+  cudaStreamDestroy(ts);
+  cudaFree(d_bad);
+  cudaFree(d_status);
+  if (rc == EMU_OK) *mismatches = status ? 0xFFFFFFFFu : bad;
+  return rc;
+}
+
+extern "C" {
 
 int emu_selftest_wait_timeout(void* stream) {
   g_last_error.clear();

@@ -271,6 +271,23 @@ int emu_tile_for(int64_t M, int64_t N, int64_t K, int32_t fast_accum, int32_t sp
  */
 int emu_selftest_wait_timeout(void* stream);
 
+/*
+ * Self-test of the tensor cores as a source of exact products: on the current
+ * device, tcgen05.mma of bf16 operands (fp32 accumulator) with a B operand whose
+ * every column has one nonzero k, so that each output is one product of two
+ * pre-scaled FP8 values; over the four format pairs, every pair of finite codes meets
+ * once.  *mismatches (caller-owned) = outputs whose bits differ from the exact fp32
+ * product (0: the tensor cores return exact products; a zero product may carry
+ * either sign), or 0xFFFFFFFF if a completion wait gave up.  Synchronous; allocates
+ * and frees two words of device memory.  Returns EMU_OK, EMU_EINVAL (null pointer) or
+ * EMU_ECUDA.  ("User guide" section 6 and "Limitations of mmaemu v0.1": the pages'
+ * tensor-core kernels rely on properties of the tensor cores; this is the check of
+ * the one property a product path needs.)  The W tile takes its products from the
+ * tensor cores only when the environment has EMU_FP8_TC=1 and this test, run once
+ * per device on first use, finds no mismatch; otherwise it computes them itself.
+ */
+int emu_tc_selftest(uint32_t* mismatches);
+
 /* Message of the last error returned on the calling host thread ("" if none). */
 const char* emu_last_error(void);
 

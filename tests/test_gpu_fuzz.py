@@ -12,7 +12,8 @@ import pytest
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-TILES = ["auto", "M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L", "W"]
+# "W:TC": the W tile with tensor-core products (opt-in, EMU_FP8_TC=1)
+TILES = ["auto", "M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L", "W", "W:TC"]
 
 CHILD = r'''
 import sys
@@ -51,8 +52,12 @@ def test_random_cases_are_bit_exact(tile):
     import __graft_entry__
     __graft_entry__.build()
     env = dict(os.environ)
-    if tile != "auto":
-        env["EMU_FP8_TILE"] = tile
+    env.pop("EMU_FP8_TC", None)
+    name, _, extra = tile.partition(":")
+    if name != "auto":
+        env["EMU_FP8_TILE"] = name
+    if extra == "TC":
+        env["EMU_FP8_TC"] = "1"
     seed = 1000 + TILES.index(tile)
     r = subprocess.run([sys.executable, "-c", CHILD, str(seed), "24"], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=900)

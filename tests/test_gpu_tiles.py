@@ -10,7 +10,8 @@ import pytest
 
 pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-TILES = ["M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L", "W"]
+# "W:TC" is the W tile with its products from the tensor cores (opt-in, EMU_FP8_TC=1)
+TILES = ["M40", "M32", "M64", "S", "K8", "K4", "K8H", "K4H", "C2", "C4", "C1", "C1L", "W", "W:TC"]
 
 CHILD = r'''
 import sys
@@ -39,6 +40,20 @@ for fast, S in ((True, 1), (False, 2)):
     a[9, 60] = 0x7C            # Inf x 0: NaN
     a[13, 200] = 0x7E          # NaN code
     assert_bits_equal(gpu_run(cs, a, b), oracle_full(cs, a, b), f"t6 fast={fast} S={S}")
+# an E4M3FN A with NaN codes against an E5M2 B with Inf and NaN codes (the W tile's
+# tensor-core products: a NaN in A meets the expanded B's zeros)
+for fast, S in ((True, 1), (True, 2)):
+    cs = W.Case("t7", 140, 80, 576, "e4m3fn", "e5m2", "bf16", fast_accum=fast, split_S=S, seed=7)
+    a, b = W.make_inputs(cs)
+    a[3, 17] = 0x7F            # NaN
+    a[100, 300] = 0xFF         # NaN
+    b[5, 40] = 0x7C            # +Inf
+    b[9, 41] = 0xFC            # -Inf
+    b[9, 200] = 0x7C           # +Inf and -Inf in one column: NaN
+    b[20, 64] = 0x7D           # NaN
+    a[:, 500] = 0x00
+    b[30, 500] = 0x7C          # Inf x 0: NaN
+    assert_bits_equal(gpu_run(cs, a, b), oracle_full(cs, a, b), f"t7 fast={fast} S={S}")
 print("ok")
 '''
 
@@ -47,7 +62,11 @@ print("ok")
 def test_forced_tile_is_bit_exact(tile):
     import __graft_entry__
     __graft_entry__.build()
-    env = dict(os.environ, EMU_FP8_TILE=tile)
+    name, _, extra = tile.partition(":")
+    env = dict(os.environ, EMU_FP8_TILE=name)
+    env.pop("EMU_FP8_TC", None)
+    if extra == "TC":
+        env["EMU_FP8_TC"] = "1"
     r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-3000:]

@@ -104,10 +104,14 @@ def kernel_source_hash() -> str:
 
 def profile_summary(workload: str):
     """The committed ncu summary of this workload's GEMM launch (profiles/<kernel>_<workload>.md,
-    the kernel emu_gemm or emu_chain), if it was taken on the current kernel sources:
-    {"traffic": DRAM bytes per launch, "ncu": {...}}."""
+    the kernel emu_gemm, emu_chain, emu_wsp, or emu_wst for the W tile with tensor-core
+    products, which runs only with EMU_FP8_TC=1), if it was taken on the current kernel
+    sources: {"traffic": DRAM bytes per launch, "ncu": {...}}."""
     import glob
     paths = sorted(glob.glob(os.path.join(ROOT, "profiles", f"emu_*_{workload}.md")))
+    tc = os.environ.get("EMU_FP8_TC") == "1"
+    wst = [p for p in paths if os.path.basename(p).startswith("emu_wst_")]
+    paths = wst if (tc and wst) else [p for p in paths if p not in wst]
     if not paths:
         return None
     for path in paths:

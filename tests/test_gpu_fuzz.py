@@ -22,6 +22,7 @@ sys.path.insert(0, "tests")
 from bit_exact_fp8_gb300 import workloads as W
 from helpers import assert_bits_equal, gpu_run, oracle_full
 seed, count = int(sys.argv[1]), int(sys.argv[2])
+wide = len(sys.argv) > 3 and sys.argv[3] == "wide"     # several CTAs of the large tiles
 rng = np.random.default_rng(seed)
 pairs = [("e4m3fn", "e4m3fn"), ("e4m3fn", "e5m2"), ("e5m2", "e4m3fn")]
 for i in range(count):
@@ -31,9 +32,9 @@ for i in range(count):
     if out == "e5m2" and fa == fb == "e4m3fn":
         out = "e4m3fn"                                   # refused by cuBLASLt
     sr = float(rng.choice([0.25, 3.0, -1.5])) if out in ("e4m3fn", "e5m2") and rng.integers(2) else None
-    M = int(rng.integers(1, 100))
-    N = 16 * int(rng.integers(1, 9))
-    K = 16 * int(rng.integers(1, 160))
+    M = int(rng.integers(1, 400 if wide else 100))
+    N = 16 * int(rng.integers(1, 25 if wide else 9))
+    K = 16 * int(rng.integers(1, 80 if wide else 160))
     S = int(rng.choice([1, 1, 2, 3, 5]))
     cs = W.Case(f"fuzz{seed}-{i}", M, N, K, fa, fb, out, fast_accum=bool(rng.integers(2)),
                 split_S=S, preset=preset, gen=("gauss", "mixed")[rng.integers(2)],
@@ -47,8 +48,7 @@ print("ok")
 '''
 
 
-@pytest.mark.parametrize("tile", TILES)
-def test_random_cases_are_bit_exact(tile):
+def _run(tile, seed, count, *extra_args):
     import __graft_entry__
     __graft_entry__.build()
     env = dict(os.environ)
@@ -58,7 +58,17 @@ def test_random_cases_are_bit_exact(tile):
         env["EMU_FP8_TILE"] = name
     if extra == "TC":
         env["EMU_FP8_TC"] = "1"
-    seed = 1000 + TILES.index(tile)
-    r = subprocess.run([sys.executable, "-c", CHILD, str(seed), "24"], cwd=ROOT, env=env,
-                       capture_output=True, text=True, timeout=900)
+    r = subprocess.run([sys.executable, "-c", CHILD, str(seed), str(count), *extra_args], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-3000:]
+
+
+@pytest.mark.parametrize("tile", TILES)
+def test_random_cases_are_bit_exact(tile):
+    _run(tile, 1000 + TILES.index(tile), 100)
+
+
+# M up to 399 and N up to 384: several CTAs of every tile, ragged in both directions
+@pytest.mark.parametrize("tile", TILES)
+def test_random_wide_cases_are_bit_exact(tile):
+    _run(tile, 2000 + TILES.index(tile), 12, "wide")
